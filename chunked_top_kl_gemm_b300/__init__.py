@@ -1,0 +1,236 @@
+"""Python binding of ``libkdtopk.so``: the fused chunked top-K KL loss on B300.
+
+Argument marshalling only.  Every step of the loss runs in the library's
+CUDA kernels; PyTorch provides device memory and the current stream.  If
+the library is missing this module raises on first use -- there is no CPU
+fallback.
+
+The C entry points are exposed under the same names
+(``kd_topk_kl_fwd_bwd``, ``kd_topk_kl_fwd_bwd_ex``,
+``kd_topk_kl_workspace_size``, ``kd_topk_kl_debug``, ``kd_gemm_bf16_test``,
+``kd_status_string``); ``fwd_bwd`` is the convenience wrapper that
+allocates outputs and the workspace with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkdtopk.so")
+HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "kd_topk_kl.h")
+
+KD_OK = 0
+STATUS_NAMES = {
+    0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_ALIGNMENT", 3: "KD_ERR_INDEX",
+    4: "KD_ERR_OOM", 5: "KD_ERR_CUDA", 6: "KD_ERR_TIMEOUT", 7: "KD_ERR_NOT_IMPLEMENTED",
+}
+
+
+class KdError(RuntimeError):
+    """A non-KD_OK status from the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{what}: {self.name} ({kd_status_string(status)})"
+                         + (f" [{last_cuda_error()}]" if status == 5 else ""))
+
+
+class _DebugOpts(ctypes.Structure):
+    _fields_ = [("lse", ctypes.c_void_p), ("zg", ctypes.c_void_p),
+                ("found_idx", ctypes.c_void_p), ("timeout_ns", ctypes.c_uint64),
+                ("inject_timeout", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libkdtopk.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m chunked_top_kl_gemm_b300._build` (there is no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                             ctypes.c_float, ctypes.c_size_t)
+    common = [vp, vp, vp, vp, i64, i32, i32, i32, f32, i32, vp, vp, vp]
+    L.kd_topk_kl_fwd_bwd.argtypes = common
+    L.kd_topk_kl_fwd_bwd.restype = i32
+    L.kd_topk_kl_fwd_bwd_ex.argtypes = common + [vp, sz, vp]
+    L.kd_topk_kl_fwd_bwd_ex.restype = i32
+    L.kd_topk_kl_debug.argtypes = common + [vp, sz, vp, ctypes.POINTER(_DebugOpts)]
+    L.kd_topk_kl_debug.restype = i32
+    L.kd_topk_kl_workspace_size.argtypes = [i64, i32, i32, i32, i32]
+    L.kd_topk_kl_workspace_size.restype = sz
+    L.kd_gemm_bf16_test.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    L.kd_gemm_bf16_test.restype = i32
+    L.kd_status_string.argtypes = [i32]
+    L.kd_status_string.restype = ctypes.c_char_p
+    L.kd_last_cuda_error.argtypes = []
+    L.kd_last_cuda_error.restype = ctypes.c_char_p
+    L.kd_abi_version.argtypes = []
+    L.kd_abi_version.restype = i32
+    _lib = L
+    return L
+
+
+def header_functions() -> list:
+    """Names of the functions ``include/kd_topk_kl.h`` declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kd_[a-z0-9_]+)\s*\(", text)))
+
+
+def kd_status_string(status: int) -> str:
+    return lib().kd_status_string(int(status)).decode()
+
+
+def last_cuda_error() -> str:
+    return lib().kd_last_cuda_error().decode()
+
+
+def abi_version() -> int:
+    return lib().kd_abi_version()
+
+
+def _check(status: int, what: str):
+    if status != KD_OK:
+        raise KdError(status, what)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check_inputs(hidden, W, topk_idx, topk_logit):
+    import torch
+    if hidden.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("hidden and W must be bfloat16")
+    if topk_idx.dtype != torch.int32:
+        raise TypeError("topk_idx must be int32 (convert torch.topk's int64 ids with .int())")
+    if topk_logit.dtype != torch.float32:
+        raise TypeError("topk_logit must be float32")
+    for name, t in (("hidden", hidden), ("W", W), ("topk_idx", topk_idx),
+                    ("topk_logit", topk_logit)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    N, H = hidden.shape
+    V, H2 = W.shape
+    if H2 != H or topk_idx.shape != topk_logit.shape or topk_idx.shape[0] != N:
+        raise ValueError("shape mismatch: hidden [N,H], W [V,H], topk_* [N,K]")
+    return N, H, V, topk_idx.shape[1]
+
+
+def kd_topk_kl_workspace_size(N: int, H: int, V: int, K: int, chunk: int) -> int:
+    return int(lib().kd_topk_kl_workspace_size(N, H, V, K, chunk))
+
+
+def kd_topk_kl_fwd_bwd(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
+                       grad_hidden, grad_W) -> float:
+    """The spec entry point: default stream, self-allocated workspace.
+
+    Writes grad_hidden / grad_W in place and returns the loss.
+    """
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    loss = ctypes.c_float(0.0)
+    st = lib().kd_topk_kl_fwd_bwd(_ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit),
+                                  N, H, V, K, float(T), int(chunk), ctypes.addressof(loss),
+                                  _ptr(grad_hidden), _ptr(grad_W))
+    _check(st, "kd_topk_kl_fwd_bwd")
+    return float(loss.value)
+
+
+def kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
+                          grad_hidden, grad_W, workspace, stream=None) -> float:
+    """Caller stream (default: torch's current stream) and workspace tensor."""
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    loss = ctypes.c_float(0.0)
+    st = lib().kd_topk_kl_fwd_bwd_ex(
+        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),
+        int(chunk), ctypes.addressof(loss), _ptr(grad_hidden), _ptr(grad_W),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd_ex")
+    return float(loss.value)
+
+
+def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad_hidden,
+                     grad_W, workspace, *, lse=None, zg=None, found_idx=None,
+                     timeout_ns: int = 0, inject_timeout: bool = False, stream=None) -> float:
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    opts = _DebugOpts(_ptr(lse) or None, _ptr(zg) or None, _ptr(found_idx) or None,
+                      int(timeout_ns), 1 if inject_timeout else 0)
+    loss = ctypes.c_float(0.0)
+    st = lib().kd_topk_kl_debug(
+        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),
+        int(chunk), ctypes.addressof(loss), _ptr(grad_hidden), _ptr(grad_W),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream),
+        ctypes.byref(opts))
+    _check(st, "kd_topk_kl_debug")
+    return float(loss.value)
+
+
+def kd_gemm_bf16_test(A, B, a_mn: bool, b_mn: bool, stream=None):
+    """C = A_op * B_op^T in fp32 (test entry of the tensor-core core)."""
+    import torch
+    if a_mn:
+        K, M = A.shape
+    else:
+        M, K = A.shape
+    if b_mn:
+        K2, N = B.shape
+    else:
+        N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("K mismatch")
+    C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    st = lib().kd_gemm_bf16_test(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(bool(a_mn)),
+                                 int(bool(b_mn)), _stream_handle(stream))
+    _check(st, "kd_gemm_bf16_test")
+    return C
+
+
+def alloc_workspace(N: int, H: int, V: int, K: int, chunk: int, device=None):
+    import torch
+    nbytes = kd_topk_kl_workspace_size(N, H, V, K, chunk)
+    if nbytes == 0:
+        raise KdError(1, "kd_topk_kl_workspace_size")
+    # torch allocations are at least 512-byte aligned
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def fwd_bwd(hidden, W, topk_idx, topk_logit, T: float = 1.0, chunk: int = 2048, *,
+            workspace=None, grad_hidden=None, grad_W=None, stream=None):
+    """Loss (float) and fp32 grad_hidden [N,H], grad_W [V,H] of the top-K KL.
+
+    Outputs and the workspace are allocated with torch on hidden's device
+    unless given.
+    """
+    import torch
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    dev = hidden.device
+    if grad_hidden is None:
+        grad_hidden = torch.empty((N, H), dtype=torch.float32, device=dev)
+    if grad_W is None:
+        grad_W = torch.empty((V, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(N, H, V, K, chunk, device=dev)
+    loss = kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T, chunk, grad_hidden,
+                                 grad_W, workspace, stream=stream)
+    return loss, grad_hidden, grad_W

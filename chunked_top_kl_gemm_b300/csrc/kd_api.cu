@@ -1,0 +1,396 @@
+// C ABI of the fused chunked top-K KL loss: argument validation, workspace
+// plan, TMA descriptors and the chunk loop (all launches on one stream).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "kd_internal.h"
+#include "../../include/kd_topk_kl.h"
+
+namespace {
+
+using kd::DevStatus;
+
+thread_local char g_last_cuda_error[256] = "";
+
+kd_status cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", where,
+                cudaGetErrorString(e));
+  return KD_ERR_CUDA;
+}
+
+#define KD_CUDA(call)                                  \
+  do {                                                 \
+    cudaError_t e_ = (call);                           \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+constexpr uint64_t kDefaultTimeoutNs = 5ull * 1000 * 1000 * 1000;
+constexpr int kMaxK = 8192;
+
+// ---------------------------------------------------------------- TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [outer][inner], 128-byte swizzled boxes of
+// box_inner x box_outer elements.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+              uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- plan
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+  long long N;
+  int H, V, K;
+  int chunk;      // rows per chunk, multiple of 128
+  int n_chunks;
+  int vt;         // vocab tiles of the forward / recompute GEMMs
+  int ht;         // hidden tiles of the gradient GEMMs
+  int splits;     // K splits of the grad_hidden GEMM
+  int sms;
+  size_t off_status, off_sid, off_sp, off_perm, off_ent, off_psum, off_loss_rows, off_lse2,
+      off_zg, off_part, off_dz, off_k4, total;
+};
+
+bool sizes_ok(long long N, int H, int V, int K, int chunk) {
+  return N >= 1 && N <= 0x7fffffffLL && H >= 8 && H % 8 == 0 && V >= 8 && V % 8 == 0 && K >= 1 &&
+         K <= V && K <= kMaxK && chunk >= 1;
+}
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 148;
+  return sms;
+}
+
+// Smallest split count whose work units fill the machine to >= 94 %, else
+// the best one, among 1..16 (and never more than the k-blocks).
+int pick_splits(int units, int kb_total, int sms) {
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= 16 && s <= kb_total; ++s) {
+    const long long u = static_cast<long long>(units) * s;
+    const double eff = static_cast<double>(u) / (cdiv(u, sms) * sms);
+    if (eff >= 0.94) return s;
+    if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
+  }
+  return best;
+}
+
+Plan make_plan(long long N, int H, int V, int K, int chunk, int sms) {
+  Plan p{};
+  p.N = N; p.H = H; p.V = V; p.K = K; p.sms = sms;
+  long long c = cdiv(chunk, 128) * 128;
+  const long long cmax = cdiv(N, 128) * 128;
+  if (c > cmax) c = cmax;
+  p.chunk = static_cast<int>(c);
+  p.n_chunks = static_cast<int>(cdiv(N, c));
+  p.vt = static_cast<int>(cdiv(V, kd::gemm_bn(kd::GV_FWD)));
+  p.ht = static_cast<int>(cdiv(H, kd::gemm_bn(kd::GV_GRAD_H)));
+  p.splits = pick_splits(static_cast<int>(c / 128) * p.ht, static_cast<int>(cdiv(V, 64)), sms);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, 256); return at; };
+  p.off_status = take(sizeof(DevStatus));
+  p.off_sid = take(sizeof(int) * N * K);
+  p.off_sp = take(sizeof(float) * N * K);
+  p.off_perm = take(sizeof(int) * N * K);
+  p.off_ent = take(sizeof(double) * N);
+  p.off_psum = take(sizeof(double) * N);
+  p.off_loss_rows = take(sizeof(double) * N);
+  p.off_lse2 = take(sizeof(float) * c);
+  p.off_zg = take(sizeof(float) * c * K);
+  p.off_part = take(sizeof(float2) * p.vt * c);
+  p.off_dz = take(2ull * c * V);
+  p.off_k4 = take(4ull * p.splits * c * H);
+  p.total = o;
+  return p;
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kd_status validate(const void* hidden, const void* W, const int32_t* idx, const float* logit,
+                   long long N, int H, int V, int K, float T, int chunk, const float* loss,
+                   const float* gh, const float* gW) {
+  if (!hidden || !W || !idx || !logit || !loss || !gh || !gW) return KD_ERR_INVALID_ARG;
+  if (!sizes_ok(N, H, V, K, chunk)) return KD_ERR_INVALID_ARG;
+  if (!(T > 0.f) || !std::isfinite(T)) return KD_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(gh, 16) || !aligned(gW, 16) ||
+      !aligned(idx, 4) || !aligned(logit, 4))
+    return KD_ERR_ALIGNMENT;
+  if (!is_device_ptr(hidden) || !is_device_ptr(W) || !is_device_ptr(idx) ||
+      !is_device_ptr(logit) || !is_device_ptr(gh) || !is_device_ptr(gW))
+    return KD_ERR_INVALID_ARG;
+  return KD_OK;
+}
+
+kd_status run(const void* hidden, const void* W, const int32_t* idx, const float* logit,
+              long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
+              float* gW, void* ws, size_t ws_bytes, cudaStream_t s, const kd_debug_opts* opts) {
+  kd_status st = validate(hidden, W, idx, logit, N, H, V, K, T, chunk, loss, gh, gW);
+  if (st != KD_OK) return st;
+  const Plan p = make_plan(N, H, V, K, chunk, device_sms());
+  if (!ws || ws_bytes < p.total) return KD_ERR_OOM;
+  if (!aligned(ws, 256)) return KD_ERR_ALIGNMENT;
+  if (!is_device_ptr(ws)) return KD_ERR_INVALID_ARG;
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  DevStatus* dst = reinterpret_cast<DevStatus*>(base + p.off_status);
+  int* sid = reinterpret_cast<int*>(base + p.off_sid);
+  float* sp = reinterpret_cast<float*>(base + p.off_sp);
+  int* perm = reinterpret_cast<int*>(base + p.off_perm);
+  double* ent = reinterpret_cast<double*>(base + p.off_ent);
+  double* psum = reinterpret_cast<double*>(base + p.off_psum);
+  double* loss_rows = reinterpret_cast<double*>(base + p.off_loss_rows);
+  float* lse2 = reinterpret_cast<float*>(base + p.off_lse2);
+  float* zg = reinterpret_cast<float*>(base + p.off_zg);
+  float2* part = reinterpret_cast<float2*>(base + p.off_part);
+  void* dz = base + p.off_dz;
+  float* k4 = reinterpret_cast<float*>(base + p.off_k4);
+
+  const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
+  float* dbg_lse = opts ? opts->lse : nullptr;
+  float* dbg_zg = opts ? opts->zg : nullptr;
+  int* dbg_found = opts ? opts->found_idx : nullptr;
+  const int inject = opts ? opts->inject_timeout : 0;
+
+  // TMA descriptors
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUtensorMap tm_hid_k, tm_w_k, tm_dz_st, tm_dz_k, tm_w_mn, tm_k4_st, tm_dz_mn, tm_hid_mn, tm_gw;
+  bool ok = true;
+  ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
+  ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, 256);
+  ok &= make_map(&tm_dz_st, BF16, 2, dz, V, p.chunk, 64, 32);
+  ok &= make_map(&tm_dz_k, BF16, 2, dz, V, p.chunk, 64, 128);
+  ok &= make_map(&tm_w_mn, BF16, 2, W, H, V, 64, 64);
+  ok &= make_map(&tm_k4_st, F32, 4, k4, H, static_cast<uint64_t>(p.splits) * p.chunk, 32, 32);
+  ok &= make_map(&tm_dz_mn, BF16, 2, dz, V, p.chunk, 64, 64);
+  ok &= make_map(&tm_hid_mn, BF16, 2, hidden, H, N, 64, 64);
+  ok &= make_map(&tm_gw, F32, 4, gW, H, V, 32, 32);
+  if (!ok) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed");
+    return KD_ERR_CUDA;
+  }
+
+  const float scale2 = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  const float alpha = static_cast<float>(1.0 / (static_cast<double>(T) * static_cast<double>(N)));
+
+  KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
+  KD_CUDA(kd::launch_prep_topk(idx, logit, N, K, V, T, sid, sp, perm, ent, psum, dst, s));
+
+  for (int j = 0; j < p.n_chunks; ++j) {
+    const int row0 = j * p.chunk;
+    const int cj = static_cast<int>(std::min<long long>(p.chunk, N - row0));
+    const int mt = static_cast<int>(cdiv(cj, 128));
+
+    kd::GemmArgs g{};
+    g.m_tiles = mt; g.n_tiles = p.vt; g.splits = 1;
+    g.kb_total = static_cast<int>(cdiv(H, 64));
+    g.order = kd::ORDER_M_FAST; g.a_row0 = row0; g.b_row0 = 0;
+    g.timeout_ns = timeout; g.status = dst; g.inject_timeout = (j == 0) ? inject : 0;
+    kd::EpiArgs e{};
+    e.rows_valid = cj; e.cols_valid = V; e.scale2 = scale2; e.alpha = 1.f;
+    e.K = K; e.grow0 = row0; e.c_alloc = p.chunk;
+    e.sid = sid; e.sp = sp; e.perm = perm; e.part = part; e.zg = zg; e.lse2 = lse2;
+    e.dbg_found = dbg_found;
+    int units = g.m_tiles * g.n_tiles;
+    KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e,
+                            std::min(units, p.sms), s));
+
+    KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, lse2,
+                                loss_rows, dbg_lse, dbg_zg, s));
+
+    g.inject_timeout = 0;
+    KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e,
+                            std::min(units, p.sms), s));
+
+    // grad_hidden rows of this chunk: split-K over the vocabulary
+    kd::GemmArgs g2{};
+    g2.m_tiles = mt; g2.n_tiles = p.ht; g2.splits = p.splits;
+    g2.kb_total = static_cast<int>(cdiv(V, 64));
+    g2.order = kd::ORDER_SPLIT; g2.a_row0 = 0; g2.b_row0 = 0;
+    g2.timeout_ns = timeout; g2.status = dst;
+    kd::EpiArgs e2{};
+    e2.rows_valid = cj; e2.cols_valid = H; e2.alpha = 1.f; e2.out_row0 = 0;
+    e2.split_rows = p.chunk;
+    units = g2.m_tiles * g2.n_tiles * g2.splits;
+    KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_dz_k, tm_w_mn, tm_k4_st, g2, e2,
+                            std::min(units, p.sms), s));
+    KD_CUDA(kd::launch_split_reduce(k4, p.splits, p.chunk, cj, H, alpha,
+                                    gh + static_cast<long long>(row0) * H, s));
+
+    // grad_W += dZ^T h_c
+    kd::GemmArgs g3{};
+    g3.m_tiles = static_cast<int>(cdiv(V, 128)); g3.n_tiles = p.ht; g3.splits = 1;
+    g3.kb_total = static_cast<int>(cdiv(cj, 64));
+    g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = row0;
+    g3.timeout_ns = timeout; g3.status = dst;
+    kd::EpiArgs e3{};
+    e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
+    e3.first = (j == 0);
+    units = g3.m_tiles * g3.n_tiles;
+    KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_hid_mn, tm_gw, g3, e3,
+                            std::min(units, p.sms), s));
+  }
+  KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s));
+
+  DevStatus hs{};
+  KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+  KD_CUDA(cudaStreamSynchronize(s));
+  if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
+  if (hs.err & kd::DEV_ERR_INDEX) return KD_ERR_INDEX;
+  *loss = static_cast<float>(hs.loss_sum / static_cast<double>(N));
+  return KD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kd_topk_kl_workspace_size(int64_t N, int H, int V, int K, int chunk) {
+  if (!sizes_ok(N, H, V, K, chunk)) return 0;
+  return make_plan(N, H, V, K, chunk, device_sms()).total;
+}
+
+kd_status kd_topk_kl_fwd_bwd_ex(const void* hidden, const void* W, const int32_t* topk_idx,
+                                const float* topk_logit, int64_t N, int H, int V, int K, float T,
+                                int chunk, float* loss, float* grad_hidden, float* grad_W,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
+             workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* topk_idx,
+                           const float* topk_logit, int64_t N, int H, int V, int K, float T,
+                           int chunk, float* loss, float* grad_hidden, float* grad_W,
+                           void* workspace, size_t workspace_bytes, void* stream,
+                           const kd_debug_opts* opts) {
+  if (opts) {
+    if ((opts->lse && !is_device_ptr(opts->lse)) || (opts->zg && !is_device_ptr(opts->zg)) ||
+        (opts->found_idx && !is_device_ptr(opts->found_idx)))
+      return KD_ERR_INVALID_ARG;
+  }
+  return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
+             workspace, workspace_bytes, static_cast<cudaStream_t>(stream), opts);
+}
+
+kd_status kd_topk_kl_fwd_bwd(const void* hidden, const void* W, const int32_t* topk_idx,
+                             const float* topk_logit, int64_t N, int H, int V, int K, float T,
+                             int chunk, float* loss, float* grad_hidden, float* grad_W) {
+  kd_status st = validate(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden,
+                          grad_W);
+  if (st != KD_OK) return st;
+  const size_t bytes = kd_topk_kl_workspace_size(N, H, V, K, chunk);
+  void* ws = nullptr;
+  cudaStream_t s = nullptr;
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return KD_ERR_OOM;
+  }
+  st = run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W, ws,
+           bytes, s, nullptr);
+  cudaError_t fe = cudaFreeAsync(ws, s);
+  if (st == KD_OK && fe != cudaSuccess) return cuda_fail(fe, "cudaFreeAsync");
+  if (st == KD_OK) {
+    cudaError_t se = cudaStreamSynchronize(s);
+    if (se != cudaSuccess) return cuda_fail(se, "cudaStreamSynchronize");
+  }
+  return st;
+}
+
+kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,
+                            int b_mn, void* stream) {
+  if (!A || !B || !C) return KD_ERR_INVALID_ARG;
+  if (M < 8 || N < 8 || K < 8 || M % 8 || N % 8 || K % 8) return KD_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return KD_ERR_ALIGNMENT;
+  if (!is_device_ptr(A) || !is_device_ptr(B) || !is_device_ptr(C)) return KD_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int variant = a_mn ? (b_mn ? kd::GV_TEST_MM : kd::GV_TEST_MK)
+                           : (b_mn ? kd::GV_TEST_KM : kd::GV_TEST_KK);
+  const int BN = kd::gemm_bn(variant);
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap ta, tb, tc;
+  bool ok = true;
+  ok &= a_mn ? make_map(&ta, BF16, 2, A, M, K, 64, 64) : make_map(&ta, BF16, 2, A, K, M, 64, 128);
+  ok &= b_mn ? make_map(&tb, BF16, 2, B, N, K, 64, 64) : make_map(&tb, BF16, 2, B, K, N, 64, BN);
+  ok &= make_map(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, 32, 32);
+  if (!ok) return KD_ERR_CUDA;
+  DevStatus* dst = nullptr;
+  KD_CUDA(cudaMallocAsync(&dst, sizeof(DevStatus), s));
+  KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
+  kd::GemmArgs g{};
+  g.m_tiles = static_cast<int>(cdiv(M, 128)); g.n_tiles = static_cast<int>(cdiv(N, BN));
+  g.splits = 1; g.kb_total = static_cast<int>(cdiv(K, 64)); g.order = kd::ORDER_M_FAST;
+  g.timeout_ns = kDefaultTimeoutNs; g.status = dst;
+  kd::EpiArgs e{};
+  e.rows_valid = M; e.cols_valid = N; e.alpha = 1.f;
+  const int units = g.m_tiles * g.n_tiles;
+  KD_CUDA(kd::launch_gemm(variant, ta, tb, tc, g, e, std::min(units, device_sms()), s));
+  DevStatus hs{};
+  KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+  KD_CUDA(cudaFreeAsync(dst, s));
+  KD_CUDA(cudaStreamSynchronize(s));
+  if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
+  return KD_OK;
+}
+
+const char* kd_status_string(kd_status s) {
+  switch (s) {
+    case KD_OK: return "ok";
+    case KD_ERR_INVALID_ARG: return "invalid argument";
+    case KD_ERR_ALIGNMENT: return "misaligned pointer";
+    case KD_ERR_INDEX: return "teacher id outside [0, V)";
+    case KD_ERR_OOM: return "out of device memory (or workspace too small)";
+    case KD_ERR_CUDA: return "CUDA error";
+    case KD_ERR_TIMEOUT: return "device-side wait timed out";
+    case KD_ERR_NOT_IMPLEMENTED: return "not implemented";
+  }
+  return "unknown status";
+}
+
+const char* kd_last_cuda_error(void) { return g_last_cuda_error; }
+
+int kd_abi_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,416 @@
+// Persistent warp-specialised tcgen05 GEMM with fused epilogues.
+//
+//   D[128 x BN tile] = A[128 x K] * B[BN x K]^T     (bf16 in, fp32 in TMEM)
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2..5  epilogue: TMEM -> registers -> fused math -> global
+// The accumulator is double-buffered in TMEM so the epilogue of one tile
+// overlaps the MMAs of the next.  Every wait is bounded (see kd_ptx.cuh):
+// on expiry the CTA raises an error bit, stops, drains what it issued,
+// frees TMEM and returns.
+//
+// Operand layouts (128-byte swizzle, 64 bf16 = 128 B per smem row):
+//   K-major  : one TMA box {64 k, rows}; rows of 128 B; 8-row atoms of 1 KB.
+//   MN-major : boxes {64 mn, 64 k} placed 8 KB apart; a row is one k.
+//
+// Epilogue kinds:
+//   EPI_FWD  : per (row, tile) online max / sum of 2^(z*log2e/T) over the
+//              valid columns, plus the gather of z at the row's cached
+//              teacher ids that fall in the tile (forward of the loss).
+//   EPI_DZ   : G = 2^(z*log2e/T - lse2) - sum of teacher p at the row's ids
+//              in the tile, stored as bf16 through TMA (backward recompute).
+//   EPI_F32  : alpha * D stored as fp32 through TMA.
+//   EPI_ACC  : alpha * D added into an fp32 tensor by TMA reduce-add
+//              (plain store when `first`).
+#pragma once
+#include "kd_args.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+
+constexpr int BM = 128;          // rows of a tile (TMEM lanes)
+constexpr int BK = 64;           // bf16 k per stage (128 B rows)
+constexpr int UMMA_K = 16;       // k of one tcgen05.mma kind::f16
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+constexpr int EPI_THREADS = 128;
+constexpr int EPI_STAGE_BYTES = 4096;   // one 32-row x 128-byte staging box
+
+template <int BN_, bool A_MN_, bool B_MN_, int STAGES_, int KIND_>
+struct GemmCfg {
+  static constexpr int BN = BN_;
+  static constexpr bool A_MN = A_MN_;
+  static constexpr bool B_MN = B_MN_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int KIND = KIND_;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  static constexpr int EPI_BYTES = (KIND == EPI_FWD) ? 0 : 4 * 2 * EPI_STAGE_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(!(KIND == EPI_FWD || KIND == EPI_DZ) || BN % 64 == 0, "BN");
+};
+
+struct Unit {
+  int m, n, s, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const GemmArgs& g) {
+  Unit t;
+  if (g.order == ORDER_M_FAST) {
+    t.m = u % g.m_tiles;
+    t.n = u / g.m_tiles;
+    t.s = 0;
+    t.kb0 = 0;
+    t.kb1 = g.kb_total;
+  } else if (g.order == ORDER_N_FAST) {
+    t.n = u % g.n_tiles;
+    t.m = u / g.n_tiles;
+    t.s = 0;
+    t.kb0 = 0;
+    t.kb1 = g.kb_total;
+  } else {
+    t.n = u % g.n_tiles;
+    const int r = u / g.n_tiles;
+    t.m = r % g.m_tiles;
+    const int s = r / g.m_tiles;
+    t.s = s;
+    t.kb0 = static_cast<int>((static_cast<long long>(s) * g.kb_total) / g.splits);
+    t.kb1 = static_cast<int>((static_cast<long long>(s + 1) * g.kb_total) / g.splits);
+  }
+  return t;
+}
+
+// Wait that ignores the abort word (used to drain work already issued).
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Number of ids of the sorted row `ids[0..K)` that are < v.
+__device__ __forceinline__ int lower_bound_ids(const int* ids, int K, int v) {
+  int lo = 0, hi = K;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(ids + mid) < v) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// r[j] for a runtime j in [0, 32) without dynamic register indexing.
+__device__ __forceinline__ float select32(const uint32_t (&r)[32], int j) {
+  float v = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v = (i == j) ? __uint_as_float(r[i]) : v;
+  return v;
+}
+
+// Write one 128-byte row (8 x 16 B chunks) of a 32-row staging box laid out
+// with the TMA 128-byte swizzle: chunk c of row i lives at chunk c ^ (i & 7).
+__device__ __forceinline__ void stage_row_128B(uint32_t box_base, int row, const uint32_t (&w)[32]) {
+  const uint32_t rb = box_base + row * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    st_shared_v4(rb + ((c ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmO, const GemmArgs g, const EpiArgs e) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + C::STAGES * C::A_BYTES;
+  uint8_t* sEpi = sB + C::STAGES * C::B_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + C::EPI_BYTES);
+  uint64_t* full = bars;                     // [STAGES]
+  uint64_t* empty = full + C::STAGES;        // [STAGES]
+  uint64_t* tfull = empty + C::STAGES;       // [2]
+  uint64_t* tempty = tfull + 2;              // [2]
+  uint64_t* mma_done = tempty + 2;           // [1]
+  uint64_t* inj_bar = mma_done + 1;          // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(inj_bar + 1);
+  volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int units = g.m_tiles * g.n_tiles * g.splits;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], EPI_THREADS);
+    }
+    mbar_init(mma_done, 1);
+    mbar_init(inj_bar, 1);
+    *abort_word = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (C::KIND != EPI_FWD) tma_prefetch_desc(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtx w{abort_word, g.status, g.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_par = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const Unit t = unit_of(u, g);
+        bool ok = true;
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (*abort_word || !mbar_wait(&empty[stage], phase ^ 1u, w, SITE_PROD)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          uint8_t* a = sA + stage * C::A_BYTES;
+          uint8_t* b = sB + stage * C::B_BYTES;
+          const int k0 = kb * BK;
+          if (!C::A_MN) {
+            tma_load_2d(a, &tmA, &full[stage], k0, g.a_row0 + t.m * BM);
+          } else {
+            tma_load_2d(a, &tmA, &full[stage], t.m * BM, g.a_row0 + k0);
+            tma_load_2d(a + 8192, &tmA, &full[stage], t.m * BM + 64, g.a_row0 + k0);
+          }
+          if (!C::B_MN) {
+            tma_load_2d(b, &tmB, &full[stage], k0, g.b_row0 + t.n * C::BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < C::BN / 64; ++j)
+              tma_load_2d(b + j * 8192, &tmB, &full[stage], t.n * C::BN + j * 64, g.b_row0 + k0);
+          }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // drain: every load issued has landed before the CTA may exit
+      for (int s = 0; s < C::STAGES; ++s)
+        if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_par >> s) & 1u, g.timeout_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, C::BN, C::A_MN, C::B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int lt = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++lt) {
+        const Unit t = unit_of(u, g);
+        const int acc = lt & 1;
+        const uint32_t acc_par = (lt >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_par ^ 1u, w, SITE_MMA_TEMPTY)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * C::BN;
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, w, SITE_MMA_FULL)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t ad = C::A_MN ? sdesc_sw128(a + kk * 2048, 8192, 1024)
+                                        : sdesc_sw128(a + kk * 32, 16, 1024);
+            const uint64_t bd = C::B_MN ? sdesc_sw128(b + kk * 2048, 8192, 1024)
+                                        : sdesc_sw128(b + kk * 32, 16, 1024);
+            tc_mma_bf16(d, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+      // drain: all MMAs issued by this thread complete before TMEM is freed
+      tc_commit(mma_done);
+      mbar_wait_drain(mma_done, 0, g.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int row = q * 32 + lane;          // row of the tile
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t stage_base = smem_u32(sEpi) + (warp - EPI_WARP0) * 2 * EPI_STAGE_BYTES;
+    uint32_t sub_ctr = 0;
+    bool ok = true;
+    if (g.inject_timeout) {
+      ok = mbar_wait(inj_bar, 0, w, SITE_INJECT);
+    }
+    int lt = 0;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++lt) {
+      const Unit t = unit_of(u, g);
+      const int acc = lt & 1;
+      const uint32_t acc_par = (lt >> 1) & 1;
+      const int mrow = t.m * BM + row;                  // row within the launch's M range
+      const bool row_ok = mrow < e.rows_valid;
+
+      // per-row teacher lookups, issued before waiting on the accumulator
+      int hit = 0, hit_end = 0, hit_col = 1 << 30;
+      const int* ids = nullptr;
+      float lse2 = 0.f;
+      const int v0 = t.n * C::BN;
+      if constexpr (C::KIND == EPI_FWD || C::KIND == EPI_DZ) {
+        if (row_ok) {
+          ids = e.sid + static_cast<long long>(e.grow0 + mrow) * e.K;
+          hit = lower_bound_ids(ids, e.K, v0);
+          hit_end = lower_bound_ids(ids, e.K, v0 + C::BN);
+          if (hit < hit_end) hit_col = __ldg(ids + hit) - v0;
+          if constexpr (C::KIND == EPI_DZ) lse2 = __ldg(e.lse2 + mrow);
+        }
+      }
+
+      bool got = mbar_wait(&tfull[acc], acc_par, w, SITE_EPI);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) { ok = false; break; }
+      tc_fence_after();
+      __syncwarp();
+      const uint32_t tb = tmem_base + lane_off + acc * C::BN;
+
+      if constexpr (C::KIND == EPI_FWD) {
+        float m_run = -INFINITY, s_run = 0.f;
+#pragma unroll 1
+        for (int b = 0; b < C::BN / 32; ++b) {
+          uint32_t r[32];
+          tmem_ld32(tb + b * 32, r);
+          tmem_ld_wait();
+          reg_fence(r);
+          const int c0 = b * 32;
+          // gather z at the cached ids that fall in these 32 columns
+          while (hit_col < c0 + 32) {
+            const float z = select32(r, hit_col - c0);
+            e.zg[static_cast<long long>(mrow) * e.K + hit] = z;
+            if (e.dbg_found) {
+              const long long gr = static_cast<long long>(e.grow0 + mrow) * e.K;
+              e.dbg_found[gr + __ldg(e.perm + gr + hit)] = v0 + hit_col;
+            }
+            ++hit;
+            hit_col = (hit < hit_end) ? __ldg(ids + hit) - v0 : (1 << 30);
+          }
+          const int nvalid = e.cols_valid - (v0 + c0);   // warp-uniform
+          if (nvalid <= 0) continue;
+          float bm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nvalid) bm = fmaxf(bm, __uint_as_float(r[j]));
+          const float m_new = fmaxf(m_run, bm * e.scale2);
+          float s = s_run * ex2_approx(m_run - m_new);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nvalid) s += ex2_approx(fmaf(__uint_as_float(r[j]), e.scale2, -m_new));
+          s_run = s;
+          m_run = m_new;
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        if (row_ok) e.part[static_cast<long long>(t.n) * e.c_alloc + mrow] = make_float2(m_run, s_run);
+      } else if constexpr (C::KIND == EPI_DZ) {
+#pragma unroll 1
+        for (int sb = 0; sb < C::BN / 64; ++sb) {
+          const int c0 = sb * 64;
+          if (v0 + c0 >= e.cols_valid) break;            // warp-uniform
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tb + c0, r0);
+          tmem_ld32(tb + c0 + 32, r1);
+          tmem_ld_wait();
+          reg_fence(r0);
+          reg_fence(r1);
+          float gv[64];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            gv[j] = row_ok ? ex2_approx(fmaf(__uint_as_float(r0[j]), e.scale2, -lse2)) : 0.f;
+            gv[32 + j] = row_ok ? ex2_approx(fmaf(__uint_as_float(r1[j]), e.scale2, -lse2)) : 0.f;
+          }
+          while (hit_col < c0 + 64) {
+            const float p = __ldg(e.sp + static_cast<long long>(e.grow0 + mrow) * e.K + hit);
+            const int jj = hit_col - c0;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) gv[j] -= (j == jj) ? p : 0.f;
+            ++hit;
+            hit_col = (hit < hit_end) ? __ldg(ids + hit) - v0 : (1 << 30);
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(gv[2 * j], gv[2 * j + 1]);
+          const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_128B(box, lane, pk);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, t.m * BM + q * 32);
+            bulk_commit();
+          }
+          ++sub_ctr;
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      } else {
+        // EPI_F32 / EPI_ACC: alpha * D -> fp32, 32-column boxes
+#pragma unroll 1
+        for (int sb = 0; sb < C::BN / 32; ++sb) {
+          const int c0 = sb * 32;
+          if (t.n * C::BN + c0 >= e.cols_valid) break;   // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tb + c0, r);
+          tmem_ld_wait();
+          reg_fence(r);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * e.alpha);
+          const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_128B(box, lane, r);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const void* src = sEpi + (box - smem_u32(sEpi));
+            const int x = t.n * C::BN + c0;
+            const int y = e.out_row0 + t.s * e.split_rows + t.m * BM + q * 32;
+            if (C::KIND == EPI_ACC && !e.first) tma_reduce_add_2d(&tmO, src, x, y);
+            else tma_store_2d(&tmO, src, x, y);
+            bulk_commit();
+          }
+          ++sub_ctr;
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      }
+    }
+    if (C::KIND != EPI_FWD && lane == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace kd

@@ -1,0 +1,49 @@
+// Internal interface between the C-ABI layer (kd_api.cu) and the kernels
+// (kd_kernels.cu).  Not installed; not part of the public header.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kd_args.h"
+#include "kd_ptx.cuh"
+
+namespace kd {
+
+// GEMM variants of the path (one template instantiation each).
+enum GemmVariant {
+  GV_FWD = 0,       // K1: hidden_c * W^T, forward epilogue (lse partials + gather)
+  GV_DZ = 1,        // K3: hidden_c * W^T recomputed, dZ epilogue (bf16 store)
+  GV_GRAD_H = 2,    // K4: dZ * W (B MN-major), fp32 split-K partials
+  GV_GRAD_W = 3,    // K5: dZ^T * hidden_c (A and B MN-major), fp32 reduce-add
+  GV_TEST_KK = 4,   // test GEMMs: fp32 store, all four major combinations
+  GV_TEST_KM = 5,
+  GV_TEST_MK = 6,
+  GV_TEST_MM = 7,
+};
+
+// Tile width of the N dimension of each variant.
+int gemm_bn(int variant);
+// Dynamic shared memory of each variant.
+int gemm_smem(int variant);
+
+cudaError_t launch_gemm(int variant, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& o, const GemmArgs& g, const EpiArgs& e, int grid,
+                        cudaStream_t s);
+
+cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N, int K, int V,
+                             float T, int* sid, float* sp, int* perm, double* ent, double* psum,
+                             DevStatus* st, cudaStream_t s);
+
+cudaError_t launch_lse_loss(const float2* part, int n_tiles, int c_alloc, int rows_valid, int grow0,
+                            const float* zg, const float* sp, const int* perm, const double* ent,
+                            const double* psum, int K, float T, float* lse2, double* loss_rows,
+                            float* dbg_lse, float* dbg_zg, cudaStream_t s);
+
+cudaError_t launch_split_reduce(const float* part, int splits, int c_alloc, int rows_valid, int H,
+                                float alpha, float* out, cudaStream_t s);
+
+cudaError_t launch_loss_final(const double* loss_rows, long long N, DevStatus* st, cudaStream_t s);
+
+}  // namespace kd

@@ -1,0 +1,170 @@
+/*
+ * kd_topk_kl.h -- C ABI of the fused chunked top-K KL distillation loss
+ * (forward + backward) for NVIDIA B300 (sm_103a).
+ *
+ * The operation.  Multiverse Computing, "Efficient Knowledge Distillation for
+ * LLMs: Offline Top-K Logits and a Fused Chunked KL Loss", as described on
+ * its news coverage:
+ *   - the teacher's K highest logits and their token ids are computed once,
+ *     offline, and stored per position (epoka.news, "The two proposed
+ *     changes"; ainewsbank.com, "Two changes remove different bottlenecks":
+ *     K = 100 there);
+ *   - the loss projects hidden states to logits one sequence chunk at a
+ *     time, folds each chunk into the running loss and discards it, and
+ *     recomputes the chunks during the backward pass instead of storing them
+ *     (glonce.com, body, the paragraph on Multiverse's fix), so the
+ *     [tokens x vocab] logit matrix is never materialised (glonce.com,
+ *     "Key facts").
+ * The pages do not print the formula.  This library computes the standard
+ * truncated-teacher KL, with z_n = W h_n (no bias), T > 0:
+ *   p_nk    = softmax_k(topk_logit_n / T)              over the K entries
+ *   log q_nv = z_nv / T - logsumexp_v(z_n / T)          over all V
+ *   loss    = (1/N) sum_n sum_k p_nk (log p_nk - log q_{n, idx_nk})
+ *   dZ_nv   = (q_nv - sum_{k: idx_nk = v} p_nk) / (T N)
+ *   grad_hidden = dZ W,  grad_W = dZ^T hidden
+ * There is no T^2 factor; the mean is over all N tokens; repeated ids add
+ * up in dZ and give one loss term each.
+ *
+ * Arithmetic.  hidden and W are bf16; the GEMMs run on tcgen05 tensor cores
+ * with fp32 accumulation; the per-token loss terms and their sum are
+ * accumulated in double; dZ is held per chunk as bf16 scratch (chunk x V);
+ * grad_W is accumulated over chunks in fp32 in device memory.
+ *
+ * Pointers.  Unless stated otherwise every array argument is a DEVICE
+ * pointer (cudaMalloc / cudaMallocAsync / managed memory on the current
+ * device) owned by the caller; the library never frees or keeps it.  Host or
+ * unregistered pointers are rejected with KD_ERR_INVALID_ARG before any
+ * launch.  All arrays are dense and row-major.
+ *
+ * Errors.  Argument errors are detected on the host before anything is
+ * launched.  Device-side errors (an id outside [0, V), a bounded wait that
+ * ran out) are reported after the stream has been synchronised; on any
+ * error the outputs are unspecified.  Every call returns after a stream
+ * synchronisation, because `loss` is a host pointer.
+ *
+ * Thread safety.  Calls on different streams may run concurrently if they
+ * use different workspaces.
+ */
+#ifndef KD_TOPK_KL_H
+#define KD_TOPK_KL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kd_status {
+  KD_OK = 0,
+  KD_ERR_INVALID_ARG = 1,     /* a size, a null pointer, a host pointer, T <= 0 ... */
+  KD_ERR_ALIGNMENT = 2,       /* a base pointer not aligned as documented */
+  KD_ERR_INDEX = 3,           /* some topk_idx entry lies outside [0, V) */
+  KD_ERR_OOM = 4,             /* workspace allocation failed / too small */
+  KD_ERR_CUDA = 5,            /* a CUDA runtime error; see kd_last_cuda_error() */
+  KD_ERR_TIMEOUT = 6,         /* a bounded device-side wait ran out */
+  KD_ERR_NOT_IMPLEMENTED = 7
+} kd_status;
+
+/*
+ * Loss and gradients of the top-K KL loss, using the legacy default stream
+ * and a workspace the call allocates (stream-ordered) and frees itself.
+ *
+ *   hidden      bf16 [N, H]  student final hidden states (device)
+ *   W           bf16 [V, H]  LM-head weight, z = hidden W^T (device)
+ *   topk_idx    int32 [N, K] cached teacher token ids, in [0, V) (device)
+ *   topk_logit  fp32 [N, K]  cached teacher logits, paired with topk_idx
+ *   N           tokens, 1 <= N <= 2^31 - 1
+ *   H           hidden size, H % 8 == 0
+ *   V           vocabulary size, V % 8 == 0, V <= 2^31 - 1
+ *   K           cached entries per token, 1 <= K <= min(V, 8192)
+ *   T           temperature, finite and > 0
+ *   chunk       token rows per chunk (>= 1); rounded up to a multiple of 128
+ *               and capped at N rounded up likewise.  Scratch grows as
+ *               chunk x V x 2 bytes.
+ *   loss        HOST float*: the mean over the N tokens
+ *   grad_hidden fp32 [N, H] (device), overwritten
+ *   grad_W      fp32 [V, H] (device), overwritten
+ *
+ * Alignment: hidden, W, grad_hidden and grad_W 16-byte aligned; topk_idx
+ * and topk_logit 4-byte aligned.  Ids are not checked for distinctness;
+ * repeated ids follow the scatter-add reading above.
+ */
+kd_status kd_topk_kl_fwd_bwd(const void* hidden, const void* W, const int32_t* topk_idx,
+                             const float* topk_logit, int64_t N, int H, int V, int K, float T,
+                             int chunk, float* loss, float* grad_hidden, float* grad_W);
+
+/*
+ * Bytes of device workspace kd_topk_kl_fwd_bwd_ex needs for these sizes on
+ * the CURRENT device (the split of one GEMM depends on its SM count).
+ * Returns 0 when the sizes are invalid.
+ */
+size_t kd_topk_kl_workspace_size(int64_t N, int H, int V, int K, int chunk);
+
+/*
+ * As kd_topk_kl_fwd_bwd, on the caller's stream and with a caller-owned
+ * workspace of at least kd_topk_kl_workspace_size(...) bytes, 256-byte
+ * aligned (device).  `stream` is a cudaStream_t (NULL = legacy default
+ * stream).  The workspace's contents on entry do not matter; it must not be
+ * used by anything else until the call returns.
+ */
+kd_status kd_topk_kl_fwd_bwd_ex(const void* hidden, const void* W, const int32_t* topk_idx,
+                                const float* topk_logit, int64_t N, int H, int V, int K, float T,
+                                int chunk, float* loss, float* grad_hidden, float* grad_W,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Test and diagnosis options for kd_topk_kl_debug.  Each output pointer may
+ * be NULL (not written).
+ *   lse        fp32 [N]    logsumexp_v(z_n / T) (device)
+ *   zg         fp32 [N, K] z at topk_idx, in the caller's k order (device)
+ *   found_idx  int32 [N, K] the vocabulary column at which the forward
+ *              epilogue met topk_idx[n, k]; must be pre-filled by the caller
+ *              (e.g. with -1) -- it equals topk_idx exactly when every id
+ *              was gathered from the right column (device)
+ *   timeout_ns limit of every device-side wait (0 = the default, 5 s)
+ *   inject_timeout  nonzero: the first GEMM's epilogue waits on a barrier
+ *              that nothing completes, so the call must end with
+ *              KD_ERR_TIMEOUT after ~timeout_ns without hanging
+ */
+typedef struct kd_debug_opts {
+  float* lse;
+  float* zg;
+  int32_t* found_idx;
+  uint64_t timeout_ns;
+  int inject_timeout;
+} kd_debug_opts;
+
+/* kd_topk_kl_fwd_bwd_ex plus the exports and hooks of `opts` (may be NULL). */
+kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* topk_idx,
+                           const float* topk_logit, int64_t N, int H, int V, int K, float T,
+                           int chunk, float* loss, float* grad_hidden, float* grad_W,
+                           void* workspace, size_t workspace_bytes, void* stream,
+                           const kd_debug_opts* opts);
+
+/*
+ * Test entry of the tensor-core GEMM core alone (no paper counterpart; it
+ * checks the operand layouts the loss uses):  C = A * B^T with
+ *   A  bf16, [M, K] when a_mn == 0 (K contiguous) or [K, M] when a_mn != 0
+ *   B  bf16, [N, K] when b_mn == 0 or [K, N] when b_mn != 0
+ *   C  fp32 [M, N]
+ * M, N, K multiples of 8; all pointers device, 16-byte aligned.  Synchronises
+ * `stream` before returning.
+ */
+kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,
+                            int b_mn, void* stream);
+
+/* Static text for a status code. */
+const char* kd_status_string(kd_status s);
+
+/* Text of the last CUDA error this library saw on the calling thread ("" if none). */
+const char* kd_last_cuda_error(void);
+
+/* Version of this ABI (incremented on any incompatible change). */
+int kd_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_TOPK_KL_H */

@@ -1,0 +1,78 @@
+"""Error paths on the GPU, none of which faults or hangs the device.
+
+Bad ids are only ever compared by the kernels, never used as addresses,
+so an id outside [0, V) is safe to pass and must come back as
+KD_ERR_INDEX.  The timeout path uses the library's own hook: one GEMM's
+epilogue waits, with a 50 ms limit, on a barrier that nothing completes;
+the bounded wait gives up, the CTA drains and frees TMEM, and the call
+returns KD_ERR_TIMEOUT.  A normal call afterwards checks that the context
+is still usable.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import chunked_top_kl_gemm_b300 as kd
+import workloads
+from tests.gpu_util import ensure_lib, run_debug, to_device
+
+pytestmark = pytest.mark.gpu
+
+CFG = workloads.custom("err", N=200, H=64, V=512, K=8, T=1.0, chunk=128)
+
+
+def _inputs(seed=0):
+    ensure_lib()
+    return to_device(workloads.make_inputs(CFG, seed=seed))
+
+
+@pytest.mark.parametrize("bad", [-1, 512, 1 << 30])
+def test_out_of_range_id_is_reported(bad):
+    inp = _inputs()
+    inp["topk_idx"][17, 3] = bad
+    with pytest.raises(kd.KdError) as ei:
+        run_debug(inp, CFG.T, CFG.chunk)
+    assert ei.value.name == "KD_ERR_INDEX"
+
+
+def test_injected_wait_times_out_and_context_survives():
+    inp = _inputs()
+    t0 = time.time()
+    with pytest.raises(kd.KdError) as ei:
+        run_debug(inp, CFG.T, CFG.chunk, timeout_ns=50_000_000, inject=True)
+    assert ei.value.name == "KD_ERR_TIMEOUT"
+    assert time.time() - t0 < 30
+    ok = run_debug(inp, CFG.T, CFG.chunk)
+    assert np.isfinite(ok["loss"])
+    assert np.array_equal(ok["found"], inp["topk_idx"].cpu().numpy())
+
+
+def test_host_pointer_is_rejected():
+    ensure_lib()
+    inp = _inputs()
+    host_hidden = inp["hidden"].cpu()
+    gh = torch.empty((CFG.N, CFG.H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((CFG.V, CFG.H), dtype=torch.float32, device="cuda")
+    ws = kd.alloc_workspace(CFG.N, CFG.H, CFG.V, CFG.K, CFG.chunk, device="cuda")
+    L = kd.lib()
+    import ctypes
+    loss = ctypes.c_float()
+    st = L.kd_topk_kl_fwd_bwd_ex(host_hidden.data_ptr(), inp["W"].data_ptr(),
+                                 inp["topk_idx"].data_ptr(), inp["topk_logit"].data_ptr(),
+                                 CFG.N, CFG.H, CFG.V, CFG.K, CFG.T, CFG.chunk,
+                                 ctypes.addressof(loss), gh.data_ptr(), gW.data_ptr(),
+                                 ws.data_ptr(), ws.numel(), None)
+    assert st == 1
+
+
+def test_small_workspace_is_oom_status():
+    inp = _inputs()
+    gh = torch.empty((CFG.N, CFG.H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((CFG.V, CFG.H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kd.KdError) as ei:
+        kd.kd_topk_kl_fwd_bwd_ex(inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"],
+                                 CFG.T, CFG.chunk, gh, gW, ws)
+    assert ei.value.name == "KD_ERR_OOM"

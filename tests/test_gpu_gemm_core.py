@@ -1,0 +1,31 @@
+"""The tcgen05 GEMM core alone, for each operand layout the loss uses.
+
+C = A_op B_op^T with bf16 inputs and fp32 accumulation is compared with a
+float64 CPU product of the same bf16 values.  Sizes span several tiles in
+every dimension and end in ragged tails (M, N, K not multiples of the
+128 x BN x 64 tile).
+"""
+import numpy as np
+import pytest
+import torch
+
+import chunked_top_kl_gemm_b300 as kd
+from tests.gpu_util import ensure_lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 384, 192), (136, 264, 72),
+                                   (392, 520, 328)])
+def test_gemm_layouts(a_mn, b_mn, M, N, K):
+    ensure_lib()
+    g = torch.Generator().manual_seed(M * 7 + N * 3 + K + 2 * a_mn + b_mn)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    Ad = (A.t().contiguous() if a_mn else A).cuda()
+    Bd = (B.t().contiguous() if b_mn else B).cuda()
+    C = kd.kd_gemm_bf16_test(Ad, Bd, bool(a_mn), bool(b_mn)).cpu().double().numpy()
+    ref = A.double().numpy() @ B.double().numpy().T
+    err = np.abs(C - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
