@@ -1,0 +1,382 @@
+#!/usr/bin/env python
+"""Benchmark of the fused chunked top-K KL loss (forward + backward) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config gptoss32k]
+    python bench.py --impl reference ...      # the float64 CPU oracle arm
+
+A step is one call of ``kd_topk_kl_fwd_bwd_ex`` over one batch of synthetic
+tokens: the whole hot path (teacher prep, per-chunk forward GEMM with the
+logsumexp/gather epilogue, loss fold, recompute GEMM with the dZ epilogue,
+grad_hidden and grad_W GEMMs, final loss).  The default workload is the
+GPT-OSS-like head at 32,768 tokens (H=2880, V=201,088, K=100, chunk 2048),
+the configuration the pages' 32K figures and GPT-OSS 20B run refer to.
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (the loss has no cross-GPU exchange in
+this build), the timed region is bracketed by barriers and the time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s fused top-K KL fwd+bwd (N×H×V), % bf16 tensor peak, peak GiB"
+GEMM_KINDS = ("gemm_fwd_lse_gather", "gemm_bwd_dz", "gemm_grad_hidden", "gemm_grad_W")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks() -> tuple:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources, to tell whether stored counters are current."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_top_kl_gemm_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/ncu_traffic.txt if the counters were
+    taken on the current kernel sources, else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+            if (kv.get("kernel") == kernel and kv.get("workload") == workload
+                    and kv.get("src") == src):
+                return float(kv["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (200 ms)."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="kd_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", self.gpu_id],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        with open(self.path) as f:
+            rows = [[c.strip() for c in ln.split(",")] for ln in f if ln.strip()]
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, power, reasons = [], [], [], set()
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_max(value: float, device=None) -> float:
+    """Maximum of `value` over ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def throughput(tokens_per_rank: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job tokens/s: the tokens every rank processed over the slowest rank's time."""
+    return tokens_per_rank * steps * world / seconds
+
+
+# ------------------------------------------------------------------ oracle legs
+def oracle_sample_rate(inp_cpu: dict, T: float, sample: int) -> dict:
+    """Time the float64 oracle on the first `sample` tokens (tokens/s)."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((d.get("num_threads", 0) for d in threadpool_info()), default=0)
+    except Exception:  # pragma: no cover
+        threads = 0
+    threads = threads or os.cpu_count()
+    t0 = time.perf_counter()
+    oracle.fused_topk_kl(inp_cpu["hidden"][:sample], inp_cpu["W"], inp_cpu["topk_idx"][:sample],
+                         inp_cpu["topk_logit"][:sample], T)
+    dt = time.perf_counter() - t0
+    return {"value": sample / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "seconds": dt, "tokens": sample}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import workloads
+    cfg = workloads.CONFIGS[args.config]
+    sample = args.ref_sample
+    inp = workloads.make_inputs(cfg, seed=0, n_rows=sample)
+    for _ in range(args.warmup):
+        oracle_sample_rate(inp, cfg.T, sample)
+    t0 = time.perf_counter()
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample_rate(inp, cfg.T, sample)
+    dt = time.perf_counter() - t0
+    value = sample * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "N": cfg.N, "H": cfg.H, "V": cfg.V, "K": cfg.K,
+                   "T": cfg.T, "chunk": cfg.chunk,
+                   "step": f"oracle over {sample} of the workload's tokens (full V, full W)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last["cores"],
+                         "kind": "oracle",
+                         "sample": f"{sample} tokens of {cfg.name} per step, float64 numpy"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main arm
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import chunked_top_kl_gemm_b300 as kd
+    import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    kd.lib()  # fail loudly if the library is missing
+
+    cfg = workloads.CONFIGS[args.config]
+    if args.tokens:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, N=args.tokens, name=f"{cfg.name}_n{args.tokens}")
+    chunk = args.chunk or cfg.chunk
+    N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    inp = workloads.make_inputs(cfg, seed=rank, device=dev)
+    h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
+    gh = torch.empty((N, H), dtype=torch.float32, device=dev)
+    gW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    ws = kd.alloc_workspace(N, H, V, K, chunk, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    del inp
+
+    def step():
+        return kd.kd_topk_kl_fwd_bwd_ex(h, W, idx, lg, T, chunk, gh, gW, ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3) if not args.allow_short_warmup else args.warmup):
+        loss = step()
+    peak_gib = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
+
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] \
+        if "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.5)
+    kd.kd_profile_enable(True)
+    dist_barrier(dev)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        loss = step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist_barrier(dev)
+    kd.kd_profile_enable(False)
+    clk = clocks.stop()
+    prof = kd.kd_profile_read()
+    t_dev = e0.elapsed_time(e1) / 1e3
+    t_max = dist_max(t_dev, dev)
+    value = throughput(N, args.steps, world, t_max)
+    tflops = cfg.flops * args.steps / t_max / 1e12
+
+    # end to end: pinned host inputs copied in every step, loss read back
+    h_host = h.cpu().pin_memory()
+    idx_host = idx.cpu().pin_memory()
+    lg_host = lg.cpu().pin_memory()
+    h2d = h_host.numel() * 2 + idx_host.numel() * 4 + lg_host.numel() * 4
+    for _ in range(2):
+        h.copy_(h_host, non_blocking=True)
+        idx.copy_(idx_host, non_blocking=True)
+        lg.copy_(lg_host, non_blocking=True)
+        step()
+    dist_barrier(dev)
+    torch.cuda.synchronize(dev)
+    w0 = time.perf_counter()
+    for _ in range(args.steps):
+        h.copy_(h_host, non_blocking=True)
+        idx.copy_(idx_host, non_blocking=True)
+        lg.copy_(lg_host, non_blocking=True)
+        step()  # synchronises and returns the loss to the host
+    torch.cuda.synchronize(dev)
+    t_e2e = dist_max(time.perf_counter() - w0, dev)
+    dist_barrier(dev)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    gemm = {k: prof[k] for k in GEMM_KINDS if k in prof and prof[k][1] > 0}
+    dom = max(gemm, key=lambda k: gemm[k][0])
+    dom_ms, dom_launches = gemm[dom]
+    flops_per_launch = 2.0 * N * H * V / (dom_launches / args.steps)
+    achieved = flops_per_launch / (dom_ms / dom_launches / 1e3) / 1e12
+    peak_sust = float(peaks["bf16_tflops_sustained"])
+    traffic = stored_traffic(dom, cfg.name)
+    launches = sum(c for _, c in prof.values())
+
+    cpu = None
+    if world == 1 and not args.skip_cpu_baseline:
+        inp_cpu = workloads.make_inputs(cfg, seed=0, n_rows=args.cpu_sample)
+        cpu = oracle_sample_rate(inp_cpu, T, args.cpu_sample)
+        cpu = {"value": cpu["value"], "unit": "tokens/s", "cores": cpu["cores"],
+               "kind": "oracle",
+               "sample": f"first {args.cpu_sample} tokens of {cfg.name} (full V and W), "
+                         f"float64 numpy, {cpu['seconds']:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "N": N, "H": H, "V": V, "K": K, "T": T,
+                   "chunk": chunk, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (W is 1.16 GB and is streamed every GEMM)"},
+        "tflops": tflops,
+        "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
+        "frac_bf16_peak_sustained": tflops / peak_sust,
+        "peak_gib": peak_gib,
+        "loss": loss,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sust,
+                     "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
+                     "frac": achieved / peak_sust, "traffic": traffic,
+                     "flops_per_launch": flops_per_launch,
+                     "avg_launch_ms": dom_ms / dom_launches},
+        "kernels": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                    for k, v in prof.items() if v[1] > 0},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": throughput(N, args.steps, world, t_e2e), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["kd", "reference"], default="kd")
+    ap.add_argument("--config", default="gptoss32k")
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (profiling captures)")
+    ap.add_argument("--cpu-sample", type=int, default=512)
+    ap.add_argument("--ref-sample", type=int, default=64)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--allow-short-warmup", action="store_true",
+                    help="profiling runs only: honour --warmup below 3")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -77,6 +77,13 @@ def lib() -> ctypes.CDLL:
     L.kd_last_cuda_error.restype = ctypes.c_char_p
     L.kd_abi_version.argtypes = []
     L.kd_abi_version.restype = i32
+    L.kd_profile_enable.argtypes = [i32]
+    L.kd_profile_enable.restype = None
+    L.kd_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_longlong), i32]
+    L.kd_profile_read.restype = i32
+    L.kd_profile_kind_name.argtypes = [i32]
+    L.kd_profile_kind_name.restype = ctypes.c_char_p
     _lib = L
     return L
 
@@ -234,3 +241,18 @@ def fwd_bwd(hidden, W, topk_idx, topk_logit, T: float = 1.0, chunk: int = 2048, 
     loss = kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T, chunk, grad_hidden,
                                  grad_W, workspace, stream=stream)
     return loss, grad_hidden, grad_W
+
+
+def kd_profile_enable(on: bool) -> None:
+    """Start (and reset) or stop the library's per-kernel event timing."""
+    lib().kd_profile_enable(1 if on else 0)
+
+
+def kd_profile_read() -> dict:
+    """{kernel kind: (total_ms, launches)} accumulated while profiling was on."""
+    L = lib()
+    n = L.kd_profile_read(None, None, 0)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_longlong * n)()
+    L.kd_profile_read(ms, cnt, n)
+    return {L.kd_profile_kind_name(i).decode(): (float(ms[i]), int(cnt[i])) for i in range(n)}

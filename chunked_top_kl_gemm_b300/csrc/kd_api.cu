@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kd_internal.h"
 #include "../../include/kd_topk_kl.h"
@@ -28,6 +29,71 @@ kd_status cuda_fail(cudaError_t e, const char* where) {
 
 constexpr uint64_t kDefaultTimeoutNs = 5ull * 1000 * 1000 * 1000;
 constexpr int kMaxK = 8192;
+
+// ---------------------------------------------------------------- profiler
+// Optional per-kernel timing: when enabled, every launch of run() is
+// bracketed by two CUDA events on the launch stream; after the call's final
+// synchronisation the elapsed times are added to per-kind totals.
+enum ProfKind { PK_PREP = 0, PK_FWD, PK_LSE, PK_DZ, PK_GRAD_H, PK_SPLIT_RED, PK_GRAD_W,
+                PK_FINAL, PK_COUNT };
+const char* const kProfNames[PK_COUNT] = {"prep_topk", "gemm_fwd_lse_gather", "lse_loss_fold",
+                                          "gemm_bwd_dz", "gemm_grad_hidden", "split_reduce",
+                                          "gemm_grad_W", "loss_final"};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  double total_ms[PK_COUNT] = {};
+  long long launches[PK_COUNT] = {};
+  // events of the call in flight (reused across calls)
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> kinds;
+  size_t used = 0;
+};
+Profiler& prof() {
+  static Profiler p;
+  return p;
+}
+
+// Bracket one launch.  Returns the index of its event pair or -1.
+struct ProfScope {
+  Profiler* p = nullptr;
+  cudaStream_t s = nullptr;
+  int slot = -1;
+  ProfScope(int kind, cudaStream_t st) {
+    Profiler& P = prof();
+    if (!P.on) return;
+    p = &P;
+    s = st;
+    if (P.ev.size() < 2 * (P.used + 1)) {
+      cudaEvent_t a, b;
+      if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) { p = nullptr; return; }
+      P.ev.push_back(a);
+      P.ev.push_back(b);
+    }
+    slot = static_cast<int>(P.used++);
+    if (P.kinds.size() < P.used) P.kinds.resize(P.used);
+    P.kinds[slot] = kind;
+    cudaEventRecord(P.ev[2 * slot], s);
+  }
+  ~ProfScope() {
+    if (p && slot >= 0) cudaEventRecord(p->ev[2 * slot + 1], s);
+  }
+};
+
+// After the stream has been synchronised: fold the call's event pairs in.
+void prof_collect() {
+  Profiler& P = prof();
+  if (!P.on) return;
+  for (size_t i = 0; i < P.used; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, P.ev[2 * i], P.ev[2 * i + 1]) == cudaSuccess) {
+      P.total_ms[P.kinds[i]] += ms;
+      P.launches[P.kinds[i]] += 1;
+    }
+  }
+  P.used = 0;
+}
 
 // ---------------------------------------------------------------- TMA descriptors
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -171,6 +237,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   if (st != KD_OK) return st;
   const Plan p = make_plan(N, H, V, K, chunk, device_sms());
   if (!ws || ws_bytes < p.total) return KD_ERR_OOM;
+  prof().used = 0;
   if (!aligned(ws, 256)) return KD_ERR_ALIGNMENT;
   if (!is_device_ptr(ws)) return KD_ERR_INVALID_ARG;
 
@@ -217,7 +284,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   const float alpha = static_cast<float>(1.0 / (static_cast<double>(T) * static_cast<double>(N)));
 
   KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
-  KD_CUDA(kd::launch_prep_topk(idx, logit, N, K, V, T, sid, sp, perm, ent, psum, dst, s));
+  { ProfScope ps_(PK_PREP, s); KD_CUDA(kd::launch_prep_topk(idx, logit, N, K, V, T, sid, sp, perm, ent, psum, dst, s)); }
 
   for (int j = 0; j < p.n_chunks; ++j) {
     const int row0 = j * p.chunk;
@@ -235,15 +302,15 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     e.sid = sid; e.sp = sp; e.perm = perm; e.part = part; e.zg = zg; e.lse2 = lse2;
     e.dbg_found = dbg_found;
     int units = g.m_tiles * g.n_tiles;
-    KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e,
-                            std::min(units, p.sms), s));
+    { ProfScope ps_(PK_FWD, s); KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e,
+                            std::min(units, p.sms), s)); }
 
-    KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, lse2,
-                                loss_rows, dbg_lse, dbg_zg, s));
+    { ProfScope ps_(PK_LSE, s); KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, lse2,
+                                loss_rows, dbg_lse, dbg_zg, s)); }
 
     g.inject_timeout = 0;
-    KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e,
-                            std::min(units, p.sms), s));
+    { ProfScope ps_(PK_DZ, s); KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e,
+                            std::min(units, p.sms), s)); }
 
     // grad_hidden rows of this chunk: split-K over the vocabulary
     kd::GemmArgs g2{};
@@ -255,10 +322,10 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     e2.rows_valid = cj; e2.cols_valid = H; e2.alpha = 1.f; e2.out_row0 = 0;
     e2.split_rows = p.chunk;
     units = g2.m_tiles * g2.n_tiles * g2.splits;
-    KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_dz_k, tm_w_mn, tm_k4_st, g2, e2,
-                            std::min(units, p.sms), s));
-    KD_CUDA(kd::launch_split_reduce(k4, p.splits, p.chunk, cj, H, alpha,
-                                    gh + static_cast<long long>(row0) * H, s));
+    { ProfScope ps_(PK_GRAD_H, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_dz_k, tm_w_mn, tm_k4_st, g2, e2,
+                            std::min(units, p.sms), s)); }
+    { ProfScope ps_(PK_SPLIT_RED, s); KD_CUDA(kd::launch_split_reduce(k4, p.splits, p.chunk, cj, H, alpha,
+                                    gh + static_cast<long long>(row0) * H, s)); }
 
     // grad_W += dZ^T h_c
     kd::GemmArgs g3{};
@@ -270,14 +337,15 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
     e3.first = (j == 0);
     units = g3.m_tiles * g3.n_tiles;
-    KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_hid_mn, tm_gw, g3, e3,
-                            std::min(units, p.sms), s));
+    { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_hid_mn, tm_gw, g3, e3,
+                            std::min(units, p.sms), s)); }
   }
-  KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s));
+  { ProfScope ps_(PK_FINAL, s); KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s)); }
 
   DevStatus hs{};
   KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
   KD_CUDA(cudaStreamSynchronize(s));
+  prof_collect();
   if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
   if (hs.err & kd::DEV_ERR_INDEX) return KD_ERR_INDEX;
   *loss = static_cast<float>(hs.loss_sum / static_cast<double>(N));
@@ -390,6 +458,31 @@ const char* kd_status_string(kd_status s) {
 }
 
 const char* kd_last_cuda_error(void) { return g_last_cuda_error; }
+
+void kd_profile_enable(int on) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  if (on && !P.on) {
+    for (int k = 0; k < PK_COUNT; ++k) { P.total_ms[k] = 0.0; P.launches[k] = 0; }
+  }
+  P.on = on != 0;
+  P.used = 0;
+}
+
+int kd_profile_read(double* total_ms, long long* launches, int max_kinds) {
+  Profiler& P = prof();
+  std::lock_guard<std::mutex> lk(P.mu);
+  const int n = max_kinds < PK_COUNT ? max_kinds : PK_COUNT;
+  for (int k = 0; k < n; ++k) {
+    if (total_ms) total_ms[k] = P.total_ms[k];
+    if (launches) launches[k] = P.launches[k];
+  }
+  return PK_COUNT;
+}
+
+const char* kd_profile_kind_name(int kind) {
+  return (kind >= 0 && kind < PK_COUNT) ? kProfNames[kind] : "";
+}
 
 int kd_abi_version(void) { return 1; }
 

@@ -154,6 +154,21 @@ kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* top
 kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,
                             int b_mn, void* stream);
 
+/*
+ * Per-kernel timing (diagnostics; no paper counterpart).  While enabled,
+ * every kernel launch of kd_topk_kl_fwd_bwd[_ex] / kd_topk_kl_debug is
+ * bracketed by two CUDA events on the call's stream, and after the call's
+ * final synchronisation the elapsed times are added to per-kind totals.
+ * kd_profile_enable(1) resets the totals; kd_profile_enable(0) stops.
+ * kd_profile_read fills up to max_kinds entries of total_ms (milliseconds)
+ * and launches (either may be NULL) and returns the number of kinds;
+ * kd_profile_kind_name names kind i.  Process-global: not for concurrent
+ * calls from several threads.
+ */
+void kd_profile_enable(int on);
+int kd_profile_read(double* total_ms, long long* launches, int max_kinds);
+const char* kd_profile_kind_name(int kind);
+
 /* Static text for a status code. */
 const char* kd_status_string(kd_status s);
 
