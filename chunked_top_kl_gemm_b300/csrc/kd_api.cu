@@ -35,10 +35,10 @@ constexpr int kMaxK = 8192;
 // bracketed by two CUDA events on the launch stream; after the call's final
 // synchronisation the elapsed times are added to per-kind totals.
 enum ProfKind { PK_PREP = 0, PK_FWD, PK_LSE, PK_DZ, PK_GRAD_H, PK_SPLIT_RED, PK_GRAD_W,
-                PK_FINAL, PK_COUNT };
+                PK_FINAL, PK_TRANSPOSE, PK_COUNT };
 const char* const kProfNames[PK_COUNT] = {"prep_topk", "gemm_fwd_lse_gather", "lse_loss_fold",
                                           "gemm_bwd_dz", "gemm_grad_hidden", "split_reduce",
-                                          "gemm_grad_W", "loss_final"};
+                                          "gemm_grad_W", "loss_final", "transpose_chunk"};
 
 struct Profiler {
   std::mutex mu;
@@ -141,11 +141,13 @@ struct Plan {
   int chunk;      // rows per chunk, multiple of 128
   int n_chunks;
   int vt;         // vocab tiles of the forward / recompute GEMMs
-  int ht;         // hidden tiles of the gradient GEMMs
-  int splits;     // K splits of the grad_hidden GEMM
+  int ht;         // hidden tiles (N) of the grad_W GEMM
+  int mth;        // hidden tiles (M) of the grad_hidden^T GEMM
+  int hp;         // mth * 128: rows of one split's grad_hidden^T partial
+  int splits;     // K splits of the grad_hidden^T GEMM
   int sms;
   size_t off_status, off_sid, off_sp, off_perm, off_ent, off_psum, off_loss_rows, off_lse2,
-      off_zg, off_part, off_dz, off_k4, total;
+      off_zg, off_part, off_dz, off_k4, off_hT, total;
 };
 
 bool sizes_ok(long long N, int H, int V, int K, int chunk) {
@@ -184,8 +186,11 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms) {
   p.chunk = static_cast<int>(c);
   p.n_chunks = static_cast<int>(cdiv(N, c));
   p.vt = static_cast<int>(cdiv(V, kd::gemm_bn(kd::GV_FWD)));
-  p.ht = static_cast<int>(cdiv(H, kd::gemm_bn(kd::GV_GRAD_H)));
-  p.splits = pick_splits(static_cast<int>(c / 128) * p.ht, static_cast<int>(cdiv(V, 64)), sms);
+  p.ht = static_cast<int>(cdiv(H, kd::gemm_bn(kd::GV_GRAD_W)));
+  p.mth = static_cast<int>(cdiv(H, 128));
+  p.hp = p.mth * 128;
+  p.splits = pick_splits(p.mth * static_cast<int>(cdiv(c, kd::gemm_bn(kd::GV_GRAD_H))),
+                         static_cast<int>(cdiv(V, 64)), sms);
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, 256); return at; };
   p.off_status = take(sizeof(DevStatus));
@@ -199,7 +204,8 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms) {
   p.off_zg = take(sizeof(float) * c * K);
   p.off_part = take(sizeof(float2) * p.vt * c);
   p.off_dz = take(2ull * c * V);
-  p.off_k4 = take(4ull * p.splits * c * H);
+  p.off_k4 = take(4ull * p.splits * p.hp * c);
+  p.off_hT = take(2ull * H * c);
   p.total = o;
   return p;
 }
@@ -254,6 +260,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   float2* part = reinterpret_cast<float2*>(base + p.off_part);
   void* dz = base + p.off_dz;
   float* k4 = reinterpret_cast<float*>(base + p.off_k4);
+  void* hT = base + p.off_hT;
 
   const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
   float* dbg_lse = opts ? opts->lse : nullptr;
@@ -264,16 +271,16 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   // TMA descriptors
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  CUtensorMap tm_hid_k, tm_w_k, tm_dz_st, tm_dz_k, tm_w_mn, tm_k4_st, tm_dz_mn, tm_hid_mn, tm_gw;
+  CUtensorMap tm_hid_k, tm_w_k, tm_dz_st, tm_dz_k256, tm_w_mn, tm_k4_st, tm_dz_mn, tm_ht_k, tm_gw;
   bool ok = true;
   ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
   ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, 256);
   ok &= make_map(&tm_dz_st, BF16, 2, dz, V, p.chunk, 64, 32);
-  ok &= make_map(&tm_dz_k, BF16, 2, dz, V, p.chunk, 64, 128);
+  ok &= make_map(&tm_dz_k256, BF16, 2, dz, V, p.chunk, 64, 256);
   ok &= make_map(&tm_w_mn, BF16, 2, W, H, V, 64, 64);
-  ok &= make_map(&tm_k4_st, F32, 4, k4, H, static_cast<uint64_t>(p.splits) * p.chunk, 32, 32);
+  ok &= make_map(&tm_k4_st, F32, 4, k4, p.chunk, static_cast<uint64_t>(p.splits) * p.hp, 32, 32);
   ok &= make_map(&tm_dz_mn, BF16, 2, dz, V, p.chunk, 64, 64);
-  ok &= make_map(&tm_hid_mn, BF16, 2, hidden, H, N, 64, 64);
+  ok &= make_map(&tm_ht_k, BF16, 2, hT, p.chunk, H, 64, 256);
   ok &= make_map(&tm_gw, F32, 4, gW, H, V, 32, 32);
   if (!ok) {
     std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed");
@@ -312,32 +319,37 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     { ProfScope ps_(PK_DZ, s); KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e,
                             std::min(units, p.sms), s)); }
 
-    // grad_hidden rows of this chunk: split-K over the vocabulary
+    // grad_hidden rows of this chunk: (dZ W)^T = W^T dZ^T, split-K over the
+    // vocabulary, then an ordered transposing reduction of the splits
     kd::GemmArgs g2{};
-    g2.m_tiles = mt; g2.n_tiles = p.ht; g2.splits = p.splits;
+    g2.m_tiles = p.mth; g2.n_tiles = static_cast<int>(cdiv(cj, kd::gemm_bn(kd::GV_GRAD_H)));
+    g2.splits = p.splits;
     g2.kb_total = static_cast<int>(cdiv(V, 64));
     g2.order = kd::ORDER_SPLIT; g2.a_row0 = 0; g2.b_row0 = 0;
     g2.timeout_ns = timeout; g2.status = dst;
     kd::EpiArgs e2{};
-    e2.rows_valid = cj; e2.cols_valid = H; e2.alpha = 1.f; e2.out_row0 = 0;
-    e2.split_rows = p.chunk;
+    e2.rows_valid = H; e2.cols_valid = cj; e2.alpha = 1.f; e2.out_row0 = 0;
+    e2.split_rows = p.hp;
     units = g2.m_tiles * g2.n_tiles * g2.splits;
-    { ProfScope ps_(PK_GRAD_H, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_dz_k, tm_w_mn, tm_k4_st, g2, e2,
+    { ProfScope ps_(PK_GRAD_H, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_w_mn, tm_dz_k256, tm_k4_st, g2, e2,
                             std::min(units, p.sms), s)); }
-    { ProfScope ps_(PK_SPLIT_RED, s); KD_CUDA(kd::launch_split_reduce(k4, p.splits, p.chunk, cj, H, alpha,
+    { ProfScope ps_(PK_SPLIT_RED, s); KD_CUDA(kd::launch_split_reduce_t(k4, p.splits,
+                                    static_cast<long long>(p.hp) * p.chunk, p.chunk, cj, H, alpha,
                                     gh + static_cast<long long>(row0) * H, s)); }
 
-    // grad_W += dZ^T h_c
+    // grad_W += dZ^T h_c   (B operand: h_c^T, K-major)
+    { ProfScope ps_(PK_TRANSPOSE, s); KD_CUDA(kd::launch_transpose_chunk(
+          static_cast<const uint8_t*>(hidden) + 2ull * row0 * H, cj, p.chunk, H, hT, s)); }
     kd::GemmArgs g3{};
     g3.m_tiles = static_cast<int>(cdiv(V, 128)); g3.n_tiles = p.ht; g3.splits = 1;
     g3.kb_total = static_cast<int>(cdiv(cj, 64));
-    g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = row0;
+    g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = 0;
     g3.timeout_ns = timeout; g3.status = dst;
     kd::EpiArgs e3{};
     e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
     e3.first = (j == 0);
     units = g3.m_tiles * g3.n_tiles;
-    { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_hid_mn, tm_gw, g3, e3,
+    { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_ht_k, tm_gw, g3, e3,
                             std::min(units, p.sms), s)); }
   }
   { ProfScope ps_(PK_FINAL, s); KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s)); }
@@ -408,14 +420,19 @@ kd_status kd_topk_kl_fwd_bwd(const void* hidden, const void* W, const int32_t* t
 }
 
 kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,
-                            int b_mn, void* stream) {
+                            int b_mn, int bn, void* stream) {
   if (!A || !B || !C) return KD_ERR_INVALID_ARG;
   if (M < 8 || N < 8 || K < 8 || M % 8 || N % 8 || K % 8) return KD_ERR_INVALID_ARG;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return KD_ERR_ALIGNMENT;
   if (!is_device_ptr(A) || !is_device_ptr(B) || !is_device_ptr(C)) return KD_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int variant = a_mn ? (b_mn ? kd::GV_TEST_MM : kd::GV_TEST_MK)
-                           : (b_mn ? kd::GV_TEST_KM : kd::GV_TEST_KK);
+  int variant = a_mn ? (b_mn ? kd::GV_TEST_MM : kd::GV_TEST_MK)
+                     : (b_mn ? kd::GV_TEST_KM : kd::GV_TEST_KK);
+  if (bn != 0 && bn != kd::gemm_bn(variant)) {
+    if (bn != 192 && bn != 256) return KD_ERR_INVALID_ARG;
+    variant = a_mn ? (b_mn ? kd::GV_TEST_MM256 : kd::GV_TEST_MK256)
+                   : (b_mn ? kd::GV_TEST_KM256 : kd::GV_TEST_KK192);
+  }
   const int BN = kd::gemm_bn(variant);
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap ta, tb, tc;

@@ -227,6 +227,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(&tempty[acc], acc_par ^ 1u, w, SITE_MMA_TEMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * C::BN;
+        // a ragged last N tile multiplies only its valid columns (rounded to 16)
+        uint32_t idesc_t = idesc;
+        const int n_rem = e.cols_valid - t.n * C::BN;
+        if (n_rem < C::BN) {
+          const int nn = n_rem <= 16 ? 16 : ((n_rem + 15) / 16) * 16;
+          idesc_t = idesc_bf16(BM, nn, C::A_MN, C::B_MN);
+        }
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, w, SITE_MMA_FULL)) { ok = false; break; }
           tc_fence_after();
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         : sdesc_sw128(a + kk * 32, 16, 1024);
             const uint64_t bd = C::B_MN ? sdesc_sw128(b + kk * 2048, 8192, 1024)
                                         : sdesc_sw128(b + kk * 32, 16, 1024);
-            tc_mma_bf16(d, ad, bd, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(d, ad, bd, idesc_t, (kb > t.kb0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }

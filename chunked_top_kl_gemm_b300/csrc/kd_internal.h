@@ -15,12 +15,16 @@ namespace kd {
 enum GemmVariant {
   GV_FWD = 0,       // K1: hidden_c * W^T, forward epilogue (lse partials + gather)
   GV_DZ = 1,        // K3: hidden_c * W^T recomputed, dZ epilogue (bf16 store)
-  GV_GRAD_H = 2,    // K4: dZ * W (B MN-major), fp32 split-K partials
-  GV_GRAD_W = 3,    // K5: dZ^T * hidden_c (A and B MN-major), fp32 reduce-add
+  GV_GRAD_H = 2,    // K4: (dZ W)^T = W^T dZ^T (A MN-major), fp32 split-K partials
+  GV_GRAD_W = 3,    // K5: dZ^T * hidden_c (A MN-major, B = h_c^T K-major), fp32 reduce-add
   GV_TEST_KK = 4,   // test GEMMs: fp32 store, all four major combinations
   GV_TEST_KM = 5,
   GV_TEST_MK = 6,
   GV_TEST_MM = 7,
+  GV_TEST_KK192 = 8,   // the same four layouts with the other tile width
+  GV_TEST_KM256 = 9,
+  GV_TEST_MK256 = 10,
+  GV_TEST_MM256 = 11,
 };
 
 // Tile width of the N dimension of each variant.
@@ -41,8 +45,12 @@ cudaError_t launch_lse_loss(const float2* part, int n_tiles, int c_alloc, int ro
                             const double* psum, int K, float T, float* lse2, double* loss_rows,
                             float* dbg_lse, float* dbg_zg, cudaStream_t s);
 
-cudaError_t launch_split_reduce(const float* part, int splits, int c_alloc, int rows_valid, int H,
-                                float alpha, float* out, cudaStream_t s);
+cudaError_t launch_split_reduce_t(const float* part, int splits, long long split_stride,
+                                  int c_alloc, int rows_valid, int H, float alpha, float* out,
+                                  cudaStream_t s);
+
+cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
+                                   cudaStream_t s);
 
 cudaError_t launch_loss_final(const double* loss_rows, long long N, DevStatus* st, cudaStream_t s);
 

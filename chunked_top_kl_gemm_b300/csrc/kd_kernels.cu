@@ -18,11 +18,14 @@
 //   lse_loss      combine the per-tile partials into logsumexp, fold the row's
 //                 KL term  sum_k p (log p - z_idx/T + lse)
 //   GEMM DZ       recompute z, G = softmax(z/T) - scatter(p) -> bf16 scratch
-//   GEMM GRAD_H   split-K  G W  -> fp32 partials;  split_reduce sums them
-//                 and scales by 1/(T N) into grad_hidden
+//   GEMM GRAD_H   split-K  (G W)^T = W^T G^T -> fp32 partials [split][H][c];
+//                 split_reduce_t sums them, transposes and scales by 1/(T N)
+//                 into grad_hidden
+//   transpose     h_c^T (bf16) for the next GEMM's K-major operand
 //   GEMM GRAD_W   G^T h_c scaled by 1/(T N), TMA reduce-added into grad_W
 //   loss_final    ordered sum of the per-token terms
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <math_constants.h>
 
 #include "kd_gemm.cuh"
@@ -32,12 +35,16 @@ namespace kd {
 
 using CfgFwd = GemmCfg<256, false, false, 4, EPI_FWD>;
 using CfgDz = GemmCfg<256, false, false, 4, EPI_DZ>;
-using CfgGradH = GemmCfg<192, false, true, 4, EPI_F32>;
-using CfgGradW = GemmCfg<192, true, true, 4, EPI_ACC>;
+using CfgGradH = GemmCfg<256, true, false, 4, EPI_F32>;   // grad_hidden^T = W^T dZ^T
+using CfgGradW = GemmCfg<256, true, false, 4, EPI_ACC>;   // grad_W = dZ^T h_c
 using CfgTestKK = GemmCfg<256, false, false, 4, EPI_F32>;
 using CfgTestKM = GemmCfg<192, false, true, 4, EPI_F32>;
 using CfgTestMK = GemmCfg<192, true, false, 4, EPI_F32>;
 using CfgTestMM = GemmCfg<192, true, true, 4, EPI_F32>;
+using CfgTestKK192 = GemmCfg<192, false, false, 4, EPI_F32>;
+using CfgTestKM256 = GemmCfg<256, false, true, 4, EPI_F32>;
+using CfgTestMK256 = GemmCfg<256, true, false, 4, EPI_F32>;
+using CfgTestMM256 = GemmCfg<256, true, true, 4, EPI_F32>;
 
 template <class C>
 static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
@@ -64,6 +71,10 @@ int gemm_bn(int variant) {
     case GV_TEST_KM: return CfgTestKM::BN;
     case GV_TEST_MK: return CfgTestMK::BN;
     case GV_TEST_MM: return CfgTestMM::BN;
+    case GV_TEST_KK192: return CfgTestKK192::BN;
+    case GV_TEST_KM256: return CfgTestKM256::BN;
+    case GV_TEST_MK256: return CfgTestMK256::BN;
+    case GV_TEST_MM256: return CfgTestMM256::BN;
   }
   return 0;
 }
@@ -78,6 +89,10 @@ int gemm_smem(int variant) {
     case GV_TEST_KM: return CfgTestKM::SMEM_BYTES;
     case GV_TEST_MK: return CfgTestMK::SMEM_BYTES;
     case GV_TEST_MM: return CfgTestMM::SMEM_BYTES;
+    case GV_TEST_KK192: return CfgTestKK192::SMEM_BYTES;
+    case GV_TEST_KM256: return CfgTestKM256::SMEM_BYTES;
+    case GV_TEST_MK256: return CfgTestMK256::SMEM_BYTES;
+    case GV_TEST_MM256: return CfgTestMM256::SMEM_BYTES;
   }
   return 0;
 }
@@ -94,6 +109,10 @@ cudaError_t launch_gemm(int variant, const CUtensorMap& a, const CUtensorMap& b,
     case GV_TEST_KM: return launch_cfg<CfgTestKM>(a, b, o, g, e, grid, s);
     case GV_TEST_MK: return launch_cfg<CfgTestMK>(a, b, o, g, e, grid, s);
     case GV_TEST_MM: return launch_cfg<CfgTestMM>(a, b, o, g, e, grid, s);
+    case GV_TEST_KK192: return launch_cfg<CfgTestKK192>(a, b, o, g, e, grid, s);
+    case GV_TEST_KM256: return launch_cfg<CfgTestKM256>(a, b, o, g, e, grid, s);
+    case GV_TEST_MK256: return launch_cfg<CfgTestMK256>(a, b, o, g, e, grid, s);
+    case GV_TEST_MM256: return launch_cfg<CfgTestMM256>(a, b, o, g, e, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -175,82 +194,149 @@ cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N
 }
 
 // ------------------------------------------------------------------ lse + loss fold
-// One thread per chunk row: combine the (max, sum) partials of every vocab
-// tile (log2 units) into lse2 = log2 sum_v 2^(z_v log2e / T), then the row's
-// KL term  sum_k p_k (log p_k - z_k/T + lse)  with lse = lse2 * ln 2.
-__global__ void __launch_bounds__(128) kd_lse_loss(
+// One block per 32 chunk rows (16 warps).  Lane l of every warp owns row
+// r0 + l; warp w combines the (max, sum) partials of vocab tiles w, w+16, ...
+// (log2 units, coalesced over the rows), then warp 0 merges the 16 results
+// into lse2 = log2 sum_v 2^(z_v log2e / T).  Each warp then folds two rows'
+// KL terms  sum_k p_k (log p_k - z_k/T + lse),  lse = lse2 ln 2,  with the
+// lanes striding over the K cached entries.
+constexpr int LSE_ROWS = 32;
+constexpr int LSE_WARPS = 16;
+
+__global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
     const float2* __restrict__ part, int n_tiles, int c_alloc, int rows_valid, int grow0,
     const float* __restrict__ zg, const float* __restrict__ sp, const int* __restrict__ perm,
     const double* __restrict__ ent, const double* __restrict__ psum, int K, double invT,
     float* __restrict__ lse2_out, double* __restrict__ loss_rows, float* __restrict__ dbg_lse,
     float* __restrict__ dbg_zg) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= rows_valid) return;
+  __shared__ float sM[LSE_WARPS][LSE_ROWS];
+  __shared__ double sS[LSE_WARPS][LSE_ROWS];
+  __shared__ double sLse[LSE_ROWS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.x * LSE_ROWS;
+  const int r = r0 + lane;
   float M = -CUDART_INF_F;
   double S = 0.0;
-  for (int t = 0; t < n_tiles; ++t) {
-    const float2 v = part[static_cast<long long>(t) * c_alloc + r];
-    if (v.x > M) {
-      S = S * static_cast<double>(exp2f(M - v.x)) + static_cast<double>(v.y);
-      M = v.x;
-    } else {
-      S += static_cast<double>(v.y) * static_cast<double>(exp2f(v.x - M));
+  if (r < rows_valid) {
+    for (int t = warp; t < n_tiles; t += LSE_WARPS) {
+      const float2 v = part[static_cast<long long>(t) * c_alloc + r];
+      if (v.x > M) {
+        S = S * static_cast<double>(exp2f(M - v.x)) + static_cast<double>(v.y);
+        M = v.x;
+      } else {
+        S += static_cast<double>(v.y) * static_cast<double>(exp2f(v.x - M));
+      }
     }
   }
-  const double lse2 = static_cast<double>(M) + log2(S);
-  lse2_out[r] = static_cast<float>(lse2);
-  const double lse = lse2 * 0.69314718055994530942;  // ln 2
-  const long long g = static_cast<long long>(grow0) + r;
-  double dot = 0.0;
-  for (int j = 0; j < K; ++j) {
-    const float z = zg[static_cast<long long>(r) * K + j];
-    dot += static_cast<double>(sp[g * K + j]) * static_cast<double>(z);
-    if (dbg_zg) dbg_zg[g * K + perm[g * K + j]] = z;
+  sM[warp][lane] = M;
+  sS[warp][lane] = S;
+  __syncthreads();
+  if (warp == 0) {
+    float Mr = -CUDART_INF_F;
+    for (int w = 0; w < LSE_WARPS; ++w) Mr = fmaxf(Mr, sM[w][lane]);
+    double Sr = 0.0;
+    for (int w = 0; w < LSE_WARPS; ++w)
+      if (sS[w][lane] > 0.0) Sr += sS[w][lane] * static_cast<double>(exp2f(sM[w][lane] - Mr));
+    const double lse2 = static_cast<double>(Mr) + log2(Sr);
+    sLse[lane] = lse2 * 0.69314718055994530942;  // ln 2
+    if (r < rows_valid) lse2_out[r] = static_cast<float>(lse2);
   }
-  loss_rows[g] = ent[g] + lse * psum[g] - dot * invT;
-  if (dbg_lse) dbg_lse[g] = static_cast<float>(lse);
+  __syncthreads();
+  for (int i = 0; i < LSE_ROWS / LSE_WARPS; ++i) {
+    const int rr = warp * (LSE_ROWS / LSE_WARPS) + i;
+    const int row = r0 + rr;
+    if (row >= rows_valid) break;
+    const long long g = static_cast<long long>(grow0) + row;
+    double dot = 0.0;
+    for (int j = lane; j < K; j += 32) {
+      const float z = zg[static_cast<long long>(row) * K + j];
+      dot += static_cast<double>(sp[g * K + j]) * static_cast<double>(z);
+      if (dbg_zg) dbg_zg[g * K + perm[g * K + j]] = z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0) {
+      loss_rows[g] = ent[g] + sLse[rr] * psum[g] - dot * invT;
+      if (dbg_lse) dbg_lse[g] = static_cast<float>(sLse[rr]);
+    }
+  }
 }
 
 cudaError_t launch_lse_loss(const float2* part, int n_tiles, int c_alloc, int rows_valid, int grow0,
                             const float* zg, const float* sp, const int* perm, const double* ent,
                             const double* psum, int K, float T, float* lse2, double* loss_rows,
                             float* dbg_lse, float* dbg_zg, cudaStream_t s) {
-  const int blocks = (rows_valid + 127) / 128;
-  kd_lse_loss<<<blocks, 128, 0, s>>>(part, n_tiles, c_alloc, rows_valid, grow0, zg, sp, perm, ent,
-                                     psum, K, 1.0 / static_cast<double>(T), lse2, loss_rows,
-                                     dbg_lse, dbg_zg);
+  const int blocks = (rows_valid + LSE_ROWS - 1) / LSE_ROWS;
+  kd_lse_loss<<<blocks, LSE_WARPS * 32, 0, s>>>(part, n_tiles, c_alloc, rows_valid, grow0, zg, sp,
+                                                perm, ent, psum, K, 1.0 / static_cast<double>(T),
+                                                lse2, loss_rows, dbg_lse, dbg_zg);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ split-K reduce
-// out[r][h] = alpha * sum_s part[s][r][h] for r < rows_valid (fixed order).
-__global__ void __launch_bounds__(256) kd_split_reduce(const float4* __restrict__ part, int splits,
-                                                       int c_alloc, int rows_valid, int H4,
-                                                       float alpha, float4* __restrict__ out) {
-  const long long total = static_cast<long long>(rows_valid) * H4;
-  const long long plane = static_cast<long long>(c_alloc) * H4;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    float4 a = part[i];
-    for (int s = 1; s < splits; ++s) {
-      const float4 b = part[s * plane + i];
-      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+// out[r][h] = alpha * sum_s part[s][h][r]  for r < rows_valid, h < H, i.e. the
+// K splits of grad_hidden^T summed in a fixed order and transposed back.
+// 32 x 32 tiles through shared memory: coalesced along r on the read side and
+// along h on the write side.
+__global__ void __launch_bounds__(256) kd_split_reduce_t(const float* __restrict__ part,
+                                                         int splits, long long split_stride,
+                                                         int c_alloc, int rows_valid, int H,
+                                                         float alpha, float* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int r0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int h = h0 + i, r = r0 + tx;
+    float a = 0.f;
+    if (h < H && r < rows_valid) {
+      const long long off = static_cast<long long>(h) * c_alloc + r;
+      a = part[off];
+      for (int sp = 1; sp < splits; ++sp) a += part[sp * split_stride + off];
     }
-    a.x *= alpha; a.y *= alpha; a.z *= alpha; a.w *= alpha;
-    out[i] = a;
+    tile[i][tx] = a * alpha;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int r = r0 + i, h = h0 + tx;
+    if (r < rows_valid && h < H) out[static_cast<long long>(r) * H + h] = tile[tx][i];
   }
 }
 
-cudaError_t launch_split_reduce(const float* part, int splits, int c_alloc, int rows_valid, int H,
-                                float alpha, float* out, cudaStream_t s) {
-  const int H4 = H / 4;
-  const long long total = static_cast<long long>(rows_valid) * H4;
-  long long blocks = (total + 255) / 256;
-  if (blocks > 148 * 8) blocks = 148 * 8;
-  if (blocks < 1) blocks = 1;
-  kd_split_reduce<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(part), splits, c_alloc, rows_valid, H4, alpha,
-      reinterpret_cast<float4*>(out));
+cudaError_t launch_split_reduce_t(const float* part, int splits, long long split_stride,
+                                  int c_alloc, int rows_valid, int H, float alpha, float* out,
+                                  cudaStream_t s) {
+  dim3 grid((rows_valid + 31) / 32, (H + 31) / 32);
+  kd_split_reduce_t<<<grid, 256, 0, s>>>(part, splits, split_stride, c_alloc, rows_valid, H,
+                                         alpha, out);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ chunk transpose
+// hT[h][r] = hidden[r][h] for r < rows_valid, 0 for rows_valid <= r < c_alloc
+// (bf16 copy, 32 x 32 tiles through shared memory).
+__global__ void __launch_bounds__(256) kd_transpose_chunk(const __nv_bfloat16* __restrict__ hid,
+                                                          int rows_valid, int c_alloc, int H,
+                                                          __nv_bfloat16* __restrict__ hT) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const int r0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int i = ty; i < 32; i += 8) {
+    const int r = r0 + i, h = h0 + tx;
+    tile[i][tx] = (r < rows_valid && h < H) ? hid[static_cast<long long>(r) * H + h]
+                                            : __float2bfloat16(0.f);
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int h = h0 + i, r = r0 + tx;
+    if (h < H && r < c_alloc) hT[static_cast<long long>(h) * c_alloc + r] = tile[tx][i];
+  }
+}
+
+cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
+                                   cudaStream_t s) {
+  dim3 grid((c_alloc + 31) / 32, (H + 31) / 32);
+  kd_transpose_chunk<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hid), rows_valid,
+                                          c_alloc, H, static_cast<__nv_bfloat16*>(hT));
   return cudaGetLastError();
 }
 

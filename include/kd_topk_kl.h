@@ -148,11 +148,12 @@ kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* top
  *   A  bf16, [M, K] when a_mn == 0 (K contiguous) or [K, M] when a_mn != 0
  *   B  bf16, [N, K] when b_mn == 0 or [K, N] when b_mn != 0
  *   C  fp32 [M, N]
- * M, N, K multiples of 8; all pointers device, 16-byte aligned.  Synchronises
- * `stream` before returning.
+ * bn selects the tile width of the N dimension (192 or 256; 0 = the width the
+ * loss uses with this layout).  M, N, K multiples of 8; all pointers device,
+ * 16-byte aligned.  Synchronises `stream` before returning.
  */
 kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,
-                            int b_mn, void* stream);
+                            int b_mn, int bn, void* stream);
 
 /*
  * Per-kernel timing (diagnostics; no paper counterpart).  While enabled,

@@ -15,17 +15,18 @@ from tests.gpu_util import ensure_lib
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("bn", [0, 192, 256])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 384, 192), (136, 264, 72),
                                    (392, 520, 328)])
-def test_gemm_layouts(a_mn, b_mn, M, N, K):
+def test_gemm_layouts(a_mn, b_mn, bn, M, N, K):
     ensure_lib()
     g = torch.Generator().manual_seed(M * 7 + N * 3 + K + 2 * a_mn + b_mn)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     B = torch.randn(N, K, generator=g).to(torch.bfloat16)
     Ad = (A.t().contiguous() if a_mn else A).cuda()
     Bd = (B.t().contiguous() if b_mn else B).cuda()
-    C = kd.kd_gemm_bf16_test(Ad, Bd, bool(a_mn), bool(b_mn)).cpu().double().numpy()
+    C = kd.kd_gemm_bf16_test(Ad, Bd, bool(a_mn), bool(b_mn), bn).cpu().double().numpy()
     ref = A.double().numpy() @ B.double().numpy().T
     err = np.abs(C - ref).max() / np.abs(ref).max()
     assert err < 1e-5, err
