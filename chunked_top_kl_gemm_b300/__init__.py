@@ -26,6 +26,7 @@ KD_OK = 0
 STATUS_NAMES = {
     0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_ALIGNMENT", 3: "KD_ERR_INDEX",
     4: "KD_ERR_OOM", 5: "KD_ERR_CUDA", 6: "KD_ERR_TIMEOUT", 7: "KD_ERR_NOT_IMPLEMENTED",
+    8: "KD_ERR_TOO_LARGE",
 }
 
 

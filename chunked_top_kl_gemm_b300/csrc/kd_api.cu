@@ -460,6 +460,70 @@ kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N
   return KD_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------- no-alloc entry
+// The scratch of kd_topk_kl_fwd_bwd_noalloc: a fixed device buffer owned by
+// the library, so that callers who may not allocate device memory can still
+// run the loss.  Host code must not pass the symbol itself to a kernel (on the
+// host it only names a stand-in object); it passes the device address looked
+// up once per device below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on
+// the first call per device).  nullptr and *st set on failure.
+void* noalloc_scratch(kd_status* st) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *st = cuda_fail(e, "cudaGetDevice");
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    *st = KD_ERR_INVALID_ARG;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      *st = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "cudaGetSymbolAddress");
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+kd_status kd_topk_kl_fwd_bwd_noalloc(const void* hidden, const void* W, const int32_t* topk_idx,
+                                     const float* topk_logit, int64_t N, int H, int V, int K,
+                                     float T, int chunk, float* loss, float* grad_hidden,
+                                     float* grad_W, void* stream) {
+  kd_status st = validate(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden,
+                          grad_W);
+  if (st != KD_OK) return st;
+  const size_t need = kd_topk_kl_workspace_size(N, H, V, K, chunk);
+  if (need == 0) return KD_ERR_INVALID_ARG;
+  if (need > KD_NOALLOC_SCRATCH_BYTES) return KD_ERR_TOO_LARGE;
+  void* ws = noalloc_scratch(&st);
+  if (!ws) return st;
+  // run() resets the status word it needs zeroed; the rest of the workspace
+  // is fully written before it is read, whatever the previous call left.
+  return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
+             ws, KD_NOALLOC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream), nullptr);
+}
+
 const char* kd_status_string(kd_status s) {
   switch (s) {
     case KD_OK: return "ok";
@@ -470,6 +534,7 @@ const char* kd_status_string(kd_status s) {
     case KD_ERR_CUDA: return "CUDA error";
     case KD_ERR_TIMEOUT: return "device-side wait timed out";
     case KD_ERR_NOT_IMPLEMENTED: return "not implemented";
+    case KD_ERR_TOO_LARGE: return "problem needs more scratch than KD_NOALLOC_SCRATCH_BYTES";
   }
   return "unknown status";
 }

@@ -63,7 +63,9 @@ typedef enum kd_status {
   KD_ERR_OOM = 4,             /* workspace allocation failed / too small */
   KD_ERR_CUDA = 5,            /* a CUDA runtime error; see kd_last_cuda_error() */
   KD_ERR_TIMEOUT = 6,         /* a bounded device-side wait ran out */
-  KD_ERR_NOT_IMPLEMENTED = 7
+  KD_ERR_NOT_IMPLEMENTED = 7,
+  KD_ERR_TOO_LARGE = 8        /* kd_topk_kl_fwd_bwd_noalloc: the problem's scratch exceeds
+                                 KD_NOALLOC_SCRATCH_BYTES */
 } kd_status;
 
 /*
@@ -169,6 +171,46 @@ kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N
 void kd_profile_enable(int on);
 int kd_profile_read(double* total_ms, long long* launches, int max_kinds);
 const char* kd_profile_kind_name(int kind);
+
+/*
+ * Size of the library's built-in scratch buffer used by
+ * kd_topk_kl_fwd_bwd_noalloc (64 MiB, held on every device that loads the
+ * library until the process exits).
+ */
+#define KD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * kd_topk_kl_fwd_bwd without any allocation (no paper counterpart).
+ *
+ * For callers that cannot allocate device memory on their own: code running
+ * where a cudaMalloc / cudaMallocAsync (or a framework allocator) is not
+ * permitted or not available, e.g. a host framework that owns every
+ * allocation, or a runtime that has already reserved all memory for its own
+ * pool.  The caller still provides the inputs and outputs exactly as for
+ * kd_topk_kl_fwd_bwd_ex; the call's workspace is a fixed buffer compiled
+ * into the library (KD_NOALLOC_SCRATCH_BYTES, 64 MiB per device).
+ *
+ *  - Sizes whose kd_topk_kl_workspace_size() exceeds KD_NOALLOC_SCRATCH_BYTES
+ *    are rejected with KD_ERR_TOO_LARGE before anything is launched.  The
+ *    scratch grows with chunk x V (the bf16 dZ of one chunk) and N x K (the
+ *    sorted teacher tables); for example N = 4096, H = 4096, V = 32,000,
+ *    K = 100 fits at chunk 256 (about 59 MiB), while a 201,088-token
+ *    vocabulary at chunk 128 and 4,096 tokens does not.
+ *  - The first call on a device looks up the buffer's device address on the
+ *    current device (cudaGetSymbolAddress); make that first call before any
+ *    stream capture.
+ *  - The buffer is shared by every call on a device and keeps the previous
+ *    call's contents; each call resets what must start at zero.  Calls whose
+ *    work overlaps on the GPU (several streams or threads at once) race on
+ *    the buffer and give wrong results: serialise them.
+ *  - No cudaMalloc, cudaFree or allocating routine is called.  Like
+ *    kd_topk_kl_fwd_bwd_ex it synchronises `stream` (a cudaStream_t, NULL =
+ *    legacy default stream) before returning.
+ */
+kd_status kd_topk_kl_fwd_bwd_noalloc(const void* hidden, const void* W, const int32_t* topk_idx,
+                                     const float* topk_logit, int64_t N, int H, int V, int K,
+                                     float T, int chunk, float* loss, float* grad_hidden,
+                                     float* grad_W, void* stream);
 
 /* Static text for a status code. */
 const char* kd_status_string(kd_status s);
