@@ -47,11 +47,15 @@ def load_peaks() -> tuple:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("kd_args.h", "kd_gemm.cuh", "kd_internal.h", "kd_kernels.cu", "kd_ptx.cuh")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources, to tell whether stored counters are current."""
+    """Hash of the device-code sources (kernels, their arguments and launch
+    helpers), to tell whether stored counters are current."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_top_kl_gemm_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

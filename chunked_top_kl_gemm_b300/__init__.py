@@ -43,7 +43,7 @@ class KdError(RuntimeError):
 class _DebugOpts(ctypes.Structure):
     _fields_ = [("lse", ctypes.c_void_p), ("zg", ctypes.c_void_p),
                 ("found_idx", ctypes.c_void_p), ("timeout_ns", ctypes.c_uint64),
-                ("inject_timeout", ctypes.c_int)]
+                ("inject_timeout", ctypes.c_int), ("loss_rows", ctypes.c_void_p)]
 
 
 _lib = None
@@ -179,11 +179,14 @@ def kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
 
 
 def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad_hidden,
-                     grad_W, workspace, *, lse=None, zg=None, found_idx=None,
+                     grad_W, workspace, *, lse=None, zg=None, found_idx=None, loss_rows=None,
                      timeout_ns: int = 0, inject_timeout: bool = False, stream=None) -> float:
+    """``kd_topk_kl_fwd_bwd_ex`` plus the debug exports (fp32 ``lse`` [N], fp32 ``zg``
+    [N,K], int32 ``found_idx`` [N,K] pre-filled by the caller, float64 ``loss_rows`` [N])
+    and the bounded-wait test hook."""
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     opts = _DebugOpts(_ptr(lse) or None, _ptr(zg) or None, _ptr(found_idx) or None,
-                      int(timeout_ns), 1 if inject_timeout else 0)
+                      int(timeout_ns), 1 if inject_timeout else 0, _ptr(loss_rows) or None)
     loss = ctypes.c_float(0.0)
     st = lib().kd_topk_kl_debug(
         _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),

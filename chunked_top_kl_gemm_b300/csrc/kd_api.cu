@@ -354,6 +354,9 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   }
   { ProfScope ps_(PK_FINAL, s); KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s)); }
 
+  if (opts && opts->loss_rows)
+    KD_CUDA(cudaMemcpyAsync(opts->loss_rows, loss_rows, sizeof(double) * N,
+                            cudaMemcpyDeviceToDevice, s));
   DevStatus hs{};
   KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
   KD_CUDA(cudaStreamSynchronize(s));
@@ -388,7 +391,8 @@ kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* top
                            const kd_debug_opts* opts) {
   if (opts) {
     if ((opts->lse && !is_device_ptr(opts->lse)) || (opts->zg && !is_device_ptr(opts->zg)) ||
-        (opts->found_idx && !is_device_ptr(opts->found_idx)))
+        (opts->found_idx && !is_device_ptr(opts->found_idx)) ||
+        (opts->loss_rows && !is_device_ptr(opts->loss_rows)))
       return KD_ERR_INVALID_ARG;
   }
   return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
@@ -566,6 +570,6 @@ const char* kd_profile_kind_name(int kind) {
   return (kind >= 0 && kind < PK_COUNT) ? kProfNames[kind] : "";
 }
 
-int kd_abi_version(void) { return 1; }
+int kd_abi_version(void) { return 2; }
 
 }  // extern "C"

@@ -124,6 +124,8 @@ kd_status kd_topk_kl_fwd_bwd_ex(const void* hidden, const void* W, const int32_t
  *              epilogue met topk_idx[n, k]; must be pre-filled by the caller
  *              (e.g. with -1) -- it equals topk_idx exactly when every id
  *              was gathered from the right column (device)
+ *   loss_rows  double [N] the per-token terms sum_k p (log p - log q_idx),
+ *              whose mean is the loss (device)
  *   timeout_ns limit of every device-side wait (0 = the default, 5 s)
  *   inject_timeout  nonzero: the first GEMM's epilogue waits on a barrier
  *              that nothing completes, so the call must end with
@@ -135,6 +137,7 @@ typedef struct kd_debug_opts {
   int32_t* found_idx;
   uint64_t timeout_ns;
   int inject_timeout;
+  double* loss_rows;
 } kd_debug_opts;
 
 /* kd_topk_kl_fwd_bwd_ex plus the exports and hooks of `opts` (may be NULL). */
