@@ -70,7 +70,7 @@ def lib() -> ctypes.CDLL:
     L.kd_topk_kl_debug.restype = i32
     L.kd_topk_kl_workspace_size.argtypes = [i64, i32, i32, i32, i32]
     L.kd_topk_kl_workspace_size.restype = sz
-    L.kd_gemm_bf16_test.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    L.kd_gemm_bf16_test.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]
     L.kd_gemm_bf16_test.restype = i32
     L.kd_status_string.argtypes = [i32]
     L.kd_status_string.restype = ctypes.c_char_p
@@ -197,8 +197,10 @@ def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad
     return float(loss.value)
 
 
-def kd_gemm_bf16_test(A, B, a_mn: bool, b_mn: bool, bn: int = 0, stream=None):
-    """C = A_op * B_op^T in fp32 (test entry of the tensor-core core)."""
+def kd_gemm_bf16_test(A, B, a_mn: bool, b_mn: bool, bn: int = 0, pair: bool = False,
+                      stream=None):
+    """C = A_op * B_op^T in fp32 (test entry of the tensor-core core); ``pair``
+    selects the CTA-pair (2-CTA MMA) form the loss uses."""
     import torch
     if a_mn:
         K, M = A.shape
@@ -212,7 +214,8 @@ def kd_gemm_bf16_test(A, B, a_mn: bool, b_mn: bool, bn: int = 0, stream=None):
         raise ValueError("K mismatch")
     C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     st = lib().kd_gemm_bf16_test(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(bool(a_mn)),
-                                 int(bool(b_mn)), int(bn), _stream_handle(stream))
+                                 int(bool(b_mn)), int(bn), int(bool(pair)),
+                                 _stream_handle(stream))
     _check(st, "kd_gemm_bf16_test")
     return C
 

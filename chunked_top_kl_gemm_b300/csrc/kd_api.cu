@@ -131,6 +131,12 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* bas
   return r == CUDA_SUCCESS;
 }
 
+// Rows of the B operand's TMA box of a GEMM variant (K-major B): the rows one
+// CTA holds, i.e. the tile width, halved on a CTA pair.
+uint32_t b_box_rows(int variant) {
+  return static_cast<uint32_t>(kd::gemm_bn(variant) / (kd::gemm_tile_m(variant) / 128));
+}
+
 // ---------------------------------------------------------------- plan
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -143,7 +149,7 @@ struct Plan {
   int vt;         // vocab tiles of the forward / recompute GEMMs
   int ht;         // hidden tiles (N) of the grad_W GEMM
   int mth;        // hidden tiles (M) of the grad_hidden^T GEMM
-  int hp;         // mth * 128: rows of one split's grad_hidden^T partial
+  int hp;         // mth * its tile M: rows of one split's grad_hidden^T partial
   int splits;     // K splits of the grad_hidden^T GEMM
   int sms;
   size_t off_status, off_sid, off_sp, off_perm, off_ent, off_psum, off_loss_rows, off_lse2,
@@ -187,10 +193,10 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms) {
   p.n_chunks = static_cast<int>(cdiv(N, c));
   p.vt = static_cast<int>(cdiv(V, kd::gemm_bn(kd::GV_FWD)));
   p.ht = static_cast<int>(cdiv(H, kd::gemm_bn(kd::GV_GRAD_W)));
-  p.mth = static_cast<int>(cdiv(H, 128));
-  p.hp = p.mth * 128;
+  p.mth = static_cast<int>(cdiv(H, kd::gemm_tile_m(kd::GV_GRAD_H)));
+  p.hp = p.mth * kd::gemm_tile_m(kd::GV_GRAD_H);
   p.splits = pick_splits(p.mth * static_cast<int>(cdiv(c, kd::gemm_bn(kd::GV_GRAD_H))),
-                         static_cast<int>(cdiv(V, 64)), sms);
+                         static_cast<int>(cdiv(V, 64)), kd::gemm_width(kd::GV_GRAD_H));
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, 256); return at; };
   p.off_status = take(sizeof(DevStatus));
@@ -274,13 +280,13 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   CUtensorMap tm_hid_k, tm_w_k, tm_dz_st, tm_dz_k256, tm_w_mn, tm_k4_st, tm_dz_mn, tm_ht_k, tm_gw;
   bool ok = true;
   ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
-  ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, 256);
+  ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, b_box_rows(kd::GV_FWD));
   ok &= make_map(&tm_dz_st, BF16, 2, dz, V, p.chunk, 64, 32);
-  ok &= make_map(&tm_dz_k256, BF16, 2, dz, V, p.chunk, 64, 256);
+  ok &= make_map(&tm_dz_k256, BF16, 2, dz, V, p.chunk, 64, b_box_rows(kd::GV_GRAD_H));
   ok &= make_map(&tm_w_mn, BF16, 2, W, H, V, 64, 64);
   ok &= make_map(&tm_k4_st, F32, 4, k4, p.chunk, static_cast<uint64_t>(p.splits) * p.hp, 32, 32);
   ok &= make_map(&tm_dz_mn, BF16, 2, dz, V, p.chunk, 64, 64);
-  ok &= make_map(&tm_ht_k, BF16, 2, hT, p.chunk, H, 64, 256);
+  ok &= make_map(&tm_ht_k, BF16, 2, hT, p.chunk, H, 64, b_box_rows(kd::GV_GRAD_W));
   ok &= make_map(&tm_gw, F32, 4, gW, H, V, 32, 32);
   if (!ok) {
     std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed");
@@ -296,7 +302,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   for (int j = 0; j < p.n_chunks; ++j) {
     const int row0 = j * p.chunk;
     const int cj = static_cast<int>(std::min<long long>(p.chunk, N - row0));
-    const int mt = static_cast<int>(cdiv(cj, 128));
+    const int mt = static_cast<int>(cdiv(cj, kd::gemm_tile_m(kd::GV_FWD)));
 
     kd::GemmArgs g{};
     g.m_tiles = mt; g.n_tiles = p.vt; g.splits = 1;
@@ -308,16 +314,13 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     e.K = K; e.grow0 = row0; e.c_alloc = p.chunk;
     e.sid = sid; e.sp = sp; e.perm = perm; e.part = part; e.zg = zg; e.lse2 = lse2;
     e.dbg_found = dbg_found;
-    int units = g.m_tiles * g.n_tiles;
-    { ProfScope ps_(PK_FWD, s); KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e,
-                            std::min(units, p.sms), s)); }
+    { ProfScope ps_(PK_FWD, s); KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e, s)); }
 
     { ProfScope ps_(PK_LSE, s); KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, lse2,
                                 loss_rows, dbg_lse, dbg_zg, s)); }
 
     g.inject_timeout = 0;
-    { ProfScope ps_(PK_DZ, s); KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e,
-                            std::min(units, p.sms), s)); }
+    { ProfScope ps_(PK_DZ, s); KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e, s)); }
 
     // grad_hidden rows of this chunk: (dZ W)^T = W^T dZ^T, split-K over the
     // vocabulary, then an ordered transposing reduction of the splits
@@ -330,9 +333,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     kd::EpiArgs e2{};
     e2.rows_valid = H; e2.cols_valid = cj; e2.alpha = 1.f; e2.out_row0 = 0;
     e2.split_rows = p.hp;
-    units = g2.m_tiles * g2.n_tiles * g2.splits;
-    { ProfScope ps_(PK_GRAD_H, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_w_mn, tm_dz_k256, tm_k4_st, g2, e2,
-                            std::min(units, p.sms), s)); }
+    { ProfScope ps_(PK_GRAD_H, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_w_mn, tm_dz_k256, tm_k4_st, g2, e2, s)); }
     { ProfScope ps_(PK_SPLIT_RED, s); KD_CUDA(kd::launch_split_reduce_t(k4, p.splits,
                                     static_cast<long long>(p.hp) * p.chunk, p.chunk, cj, H, alpha,
                                     gh + static_cast<long long>(row0) * H, s)); }
@@ -341,16 +342,15 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     { ProfScope ps_(PK_TRANSPOSE, s); KD_CUDA(kd::launch_transpose_chunk(
           static_cast<const uint8_t*>(hidden) + 2ull * row0 * H, cj, p.chunk, H, hT, s)); }
     kd::GemmArgs g3{};
-    g3.m_tiles = static_cast<int>(cdiv(V, 128)); g3.n_tiles = p.ht; g3.splits = 1;
+    g3.m_tiles = static_cast<int>(cdiv(V, kd::gemm_tile_m(kd::GV_GRAD_W))); g3.n_tiles = p.ht;
+    g3.splits = 1;
     g3.kb_total = static_cast<int>(cdiv(cj, 64));
     g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = 0;
     g3.timeout_ns = timeout; g3.status = dst;
     kd::EpiArgs e3{};
     e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
     e3.first = (j == 0);
-    units = g3.m_tiles * g3.n_tiles;
-    { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_ht_k, tm_gw, g3, e3,
-                            std::min(units, p.sms), s)); }
+    { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_ht_k, tm_gw, g3, e3, s)); }
   }
   { ProfScope ps_(PK_FINAL, s); KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s)); }
 
@@ -424,7 +424,7 @@ kd_status kd_topk_kl_fwd_bwd(const void* hidden, const void* W, const int32_t* t
 }
 
 kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,
-                            int b_mn, int bn, void* stream) {
+                            int b_mn, int bn, int pair, void* stream) {
   if (!A || !B || !C) return KD_ERR_INVALID_ARG;
   if (M < 8 || N < 8 || K < 8 || M % 8 || N % 8 || K % 8) return KD_ERR_INVALID_ARG;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return KD_ERR_ALIGNMENT;
@@ -432,30 +432,34 @@ kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int variant = a_mn ? (b_mn ? kd::GV_TEST_MM : kd::GV_TEST_MK)
                      : (b_mn ? kd::GV_TEST_KM : kd::GV_TEST_KK);
-  if (bn != 0 && bn != kd::gemm_bn(variant)) {
+  if (pair) {
+    if (bn != 0 && bn != 256) return KD_ERR_INVALID_ARG;
+    variant = a_mn ? (b_mn ? kd::GV_TEST_MM2 : kd::GV_TEST_MK2)
+                   : (b_mn ? kd::GV_TEST_KM2 : kd::GV_TEST_KK2);
+  } else if (bn != 0 && bn != kd::gemm_bn(variant)) {
     if (bn != 192 && bn != 256) return KD_ERR_INVALID_ARG;
     variant = a_mn ? (b_mn ? kd::GV_TEST_MM256 : kd::GV_TEST_MK256)
                    : (b_mn ? kd::GV_TEST_KM256 : kd::GV_TEST_KK192);
   }
-  const int BN = kd::gemm_bn(variant);
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap ta, tb, tc;
   bool ok = true;
   ok &= a_mn ? make_map(&ta, BF16, 2, A, M, K, 64, 64) : make_map(&ta, BF16, 2, A, K, M, 64, 128);
-  ok &= b_mn ? make_map(&tb, BF16, 2, B, N, K, 64, 64) : make_map(&tb, BF16, 2, B, K, N, 64, BN);
+  ok &= b_mn ? make_map(&tb, BF16, 2, B, N, K, 64, 64)
+              : make_map(&tb, BF16, 2, B, K, N, 64, b_box_rows(variant));
   ok &= make_map(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, N, M, 32, 32);
   if (!ok) return KD_ERR_CUDA;
   DevStatus* dst = nullptr;
   KD_CUDA(cudaMallocAsync(&dst, sizeof(DevStatus), s));
   KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
   kd::GemmArgs g{};
-  g.m_tiles = static_cast<int>(cdiv(M, 128)); g.n_tiles = static_cast<int>(cdiv(N, BN));
+  g.m_tiles = static_cast<int>(cdiv(M, kd::gemm_tile_m(variant)));
+  g.n_tiles = static_cast<int>(cdiv(N, kd::gemm_bn(variant)));
   g.splits = 1; g.kb_total = static_cast<int>(cdiv(K, 64)); g.order = kd::ORDER_M_FAST;
   g.timeout_ns = kDefaultTimeoutNs; g.status = dst;
   kd::EpiArgs e{};
   e.rows_valid = M; e.cols_valid = N; e.alpha = 1.f;
-  const int units = g.m_tiles * g.n_tiles;
-  KD_CUDA(kd::launch_gemm(variant, ta, tb, tc, g, e, std::min(units, device_sms()), s));
+  KD_CUDA(kd::launch_gemm(variant, ta, tb, tc, g, e, s));
   DevStatus hs{};
   KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
   KD_CUDA(cudaFreeAsync(dst, s));

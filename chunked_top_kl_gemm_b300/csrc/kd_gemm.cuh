@@ -1,6 +1,11 @@
 // Persistent warp-specialised tcgen05 GEMM with fused epilogues.
 //
-//   D[128 x BN tile] = A[128 x K] * B[BN x K]^T     (bf16 in, fp32 in TMEM)
+//   D[TILE_M x BN tile] = A[TILE_M x K] * B[BN x K]^T   (bf16 in, fp32 in TMEM)
+//
+// TILE_M is 128 (one CTA per tile) or 256 (a CTA pair per tile: each CTA
+// loads 128 rows of A and BN/2 rows of B, the leader CTA issues 2-CTA MMAs
+// and each CTA's TMEM holds its 128 rows of the accumulator).  The pair
+// halves the operand bytes each SM pulls from L2 per MMA.
 //
 // Roles (192 threads, one CTA per SM):
 //   warp 0      TMA producer: fills a STAGES-deep ring of (A, B) k-blocks
@@ -38,22 +43,28 @@ constexpr int EPI_WARP0 = 2;
 constexpr int EPI_THREADS = 128;
 constexpr int EPI_STAGE_BYTES = 4096;   // one 32-row x 128-byte staging box
 
-template <int BN_, bool A_MN_, bool B_MN_, int STAGES_, int KIND_>
+template <int BN_, bool A_MN_, bool B_MN_, int STAGES_, int KIND_, bool CTA2_ = false>
 struct GemmCfg {
-  static constexpr int BN = BN_;
+  static constexpr int BN = BN_;           // N of one accumulator tile (both CTAs of a pair)
   static constexpr bool A_MN = A_MN_;
   static constexpr bool B_MN = B_MN_;
   static constexpr int STAGES = STAGES_;
   static constexpr int KIND = KIND_;
+  static constexpr bool CTA2 = CTA2_;      // 2-CTA MMA: tile 256 x BN over a CTA pair
+  static constexpr int NCTA = CTA2 ? 2 : 1;
+  static constexpr int TILE_M = BM * NCTA; // M of one work unit
+  static constexpr int BN_CTA = BN / NCTA; // B rows one CTA loads and holds
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TX_BYTES = NCTA * STAGE_BYTES;   // one stage of the whole pair
   static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
   static constexpr int EPI_BYTES = (KIND == EPI_FWD) ? 0 : 4 * 2 * EPI_STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(!(KIND == EPI_FWD || KIND == EPI_DZ) || BN % 64 == 0, "BN");
+  static_assert(!B_MN || BN_CTA % 64 == 0, "MN-major B boxes are 64 wide");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 struct Unit {
@@ -124,6 +135,11 @@ __device__ __forceinline__ void stage_row_128B(uint32_t box_base, int row, const
   }
 }
 
+// Stage fills issued so far for ring slot s after `issued` k-blocks.
+__device__ __forceinline__ uint32_t ring_fills(uint32_t issued, int s, int stages) {
+  return issued > static_cast<uint32_t>(s) ? (issued - 1 - s) / stages + 1 : 0u;
+}
+
 template <class C>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -135,18 +151,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sB = sA + C::STAGES * C::A_BYTES;
   uint8_t* sEpi = sB + C::STAGES * C::B_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + C::EPI_BYTES);
-  uint64_t* full = bars;                     // [STAGES]
+  uint64_t* full = bars;                     // [STAGES]  (pair: used in the leader only)
   uint64_t* empty = full + C::STAGES;        // [STAGES]
   uint64_t* tfull = empty + C::STAGES;       // [2]
-  uint64_t* tempty = tfull + 2;              // [2]
+  uint64_t* tempty = tfull + 2;              // [2]       (pair: used in the leader only)
   uint64_t* mma_done = tempty + 2;           // [1]
   uint64_t* inj_bar = mma_done + 1;          // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(inj_bar + 1);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int units = g.m_tiles * g.n_tiles * g.splits;
+  // CTA pairs: rank 0 (the leader) issues the MMAs of the pair and owns the
+  // ring's full barriers and the accumulators' empty barriers.
+  const uint32_t rank = C::CTA2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit0 = C::CTA2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustep = C::CTA2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -155,85 +178,112 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], EPI_THREADS);
+      mbar_init(&tempty[a], 4 * C::NCTA);   // one arrival per epilogue warp of the pair
     }
     mbar_init(mma_done, 1);
     mbar_init(inj_bar, 1);
     *abort_word = 0;
+    *peer_issued = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (C::KIND != EPI_FWD) tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<C::NCTA>(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish<C::NCTA>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::CTA2) cluster_sync_all();   // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtx w{abort_word, g.status, g.timeout_ns};
 
+  // valid columns of tile n, rounded to what the MMA may multiply
+  auto tile_cols = [&](int n) {
+    const int rem = e.cols_valid - n * C::BN;
+    if (rem >= C::BN) return C::BN;
+    const int q = C::CTA2 ? 32 : 16;           // pair: each half a multiple of 16 rows
+    const int nn = rem <= q ? q : ((rem + q - 1) / q) * q;
+    return nn < C::BN ? nn : C::BN;
+  };
+
+  uint32_t issued = 0;   // k-blocks this CTA's producer issued (ring position)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_par = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      uint32_t phase = 0;
+      for (int u = unit0; u < units; u += ustep) {
         const Unit t = unit_of(u, g);
+        const int a_m0 = t.m * C::TILE_M + static_cast<int>(rank) * BM;
+        const int b_n0 = t.n * C::BN + static_cast<int>(rank) * (tile_cols(t.n) / C::NCTA);
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (*abort_word || !mbar_wait(&empty[stage], phase ^ 1u, w, SITE_PROD)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           uint8_t* a = sA + stage * C::A_BYTES;
           uint8_t* b = sB + stage * C::B_BYTES;
           const int k0 = kb * BK;
-          if (!C::A_MN) {
-            tma_load_2d(a, &tmA, &full[stage], k0, g.a_row0 + t.m * BM);
-          } else {
-            tma_load_2d(a, &tmA, &full[stage], t.m * BM, g.a_row0 + k0);
-            tma_load_2d(a + 8192, &tmA, &full[stage], t.m * BM + 64, g.a_row0 + k0);
-          }
-          if (!C::B_MN) {
-            tma_load_2d(b, &tmB, &full[stage], k0, g.b_row0 + t.n * C::BN);
-          } else {
+          if constexpr (!C::CTA2) {
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            if (!C::A_MN) {
+              tma_load_2d(a, &tmA, &full[stage], k0, g.a_row0 + a_m0);
+            } else {
+              tma_load_2d(a, &tmA, &full[stage], a_m0, g.a_row0 + k0);
+              tma_load_2d(a + 8192, &tmA, &full[stage], a_m0 + 64, g.a_row0 + k0);
+            }
+            if (!C::B_MN) {
+              tma_load_2d(b, &tmB, &full[stage], k0, g.b_row0 + b_n0);
+            } else {
 #pragma unroll
-            for (int j = 0; j < C::BN / 64; ++j)
-              tma_load_2d(b + j * 8192, &tmB, &full[stage], t.n * C::BN + j * 64, g.b_row0 + k0);
+              for (int j = 0; j < C::BN_CTA / 64; ++j)
+                tma_load_2d(b + j * 8192, &tmB, &full[stage], b_n0 + j * 64, g.b_row0 + k0);
+            }
+          } else {
+            // both CTAs' bytes complete on the leader's full barrier
+            if (leader) mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+            if (!C::A_MN) {
+              tma_load_2d_pair(a, &tmA, fb, k0, g.a_row0 + a_m0);
+            } else {
+              tma_load_2d_pair(a, &tmA, fb, a_m0, g.a_row0 + k0);
+              tma_load_2d_pair(a + 8192, &tmA, fb, a_m0 + 64, g.a_row0 + k0);
+            }
+            if (!C::B_MN) {
+              tma_load_2d_pair(b, &tmB, fb, k0, g.b_row0 + b_n0);
+            } else {
+#pragma unroll
+              for (int j = 0; j < C::BN_CTA / 64; ++j)
+                tma_load_2d_pair(b + j * 8192, &tmB, fb, b_n0 + j * 64, g.b_row0 + k0);
+            }
           }
+          ++issued;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
-      // drain: every load issued has landed before the CTA may exit
-      for (int s = 0; s < C::STAGES; ++s)
-        if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_par >> s) & 1u, g.timeout_ns);
+      if constexpr (C::CTA2) {
+        if (!leader) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)peer_issued), 0), issued);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, C::BN, C::A_MN, C::B_MN);
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int lt = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++lt) {
+      for (int u = unit0; u < units && ok; u += ustep, ++lt) {
         const Unit t = unit_of(u, g);
         const int acc = lt & 1;
         const uint32_t acc_par = (lt >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], acc_par ^ 1u, w, SITE_MMA_TEMPTY)) break;
+        if (!mbar_wait<C::CTA2>(&tempty[acc], acc_par ^ 1u, w, SITE_MMA_TEMPTY)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * C::BN;
-        // a ragged last N tile multiplies only its valid columns (rounded to 16)
-        uint32_t idesc_t = idesc;
-        const int n_rem = e.cols_valid - t.n * C::BN;
-        if (n_rem < C::BN) {
-          const int nn = n_rem <= 16 ? 16 : ((n_rem + 15) / 16) * 16;
-          idesc_t = idesc_bf16(BM, nn, C::A_MN, C::B_MN);
-        }
+        // a ragged last N tile multiplies only its valid columns
+        const int nn = tile_cols(t.n);
+        const uint32_t idesc_t = idesc_bf16(C::TILE_M, nn, C::A_MN, C::B_MN);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, w, SITE_MMA_FULL)) { ok = false; break; }
           tc_fence_after();
@@ -245,35 +295,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         : sdesc_sw128(a + kk * 32, 16, 1024);
             const uint64_t bd = C::B_MN ? sdesc_sw128(b + kk * 2048, 8192, 1024)
                                         : sdesc_sw128(b + kk * 32, 16, 1024);
-            tc_mma_bf16(d, ad, bd, idesc_t, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16<C::NCTA>(d, ad, bd, idesc_t, (kb > t.kb0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&empty[stage]);
+          if constexpr (C::CTA2) tc_commit_pair(&empty[stage]);
+          else tc_commit<1>(&empty[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (ok) tc_commit(&tfull[acc]);
+        if (ok) {
+          if constexpr (C::CTA2) tc_commit_pair(&tfull[acc]);
+          else tc_commit<1>(&tfull[acc]);
+        }
       }
       // drain: all MMAs issued by this thread complete before TMEM is freed
-      tc_commit(mma_done);
+      tc_commit<C::NCTA>(mma_done);
       mbar_wait_drain(mma_done, 0, g.timeout_ns);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int row = q * 32 + lane;          // row of the tile
+    const int row = q * 32 + lane;          // row of this CTA's 128-row slab
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t stage_base = smem_u32(sEpi) + (warp - EPI_WARP0) * 2 * EPI_STAGE_BYTES;
+    // where this warp reports a drained accumulator: the leader's tempty
+    const uint32_t tempty_dst[2] = {C::CTA2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u,
+                                    C::CTA2 ? mapa_shared(smem_u32(&tempty[1]), 0) : 0u};
+    auto release_acc = [&](int acc) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_remote(tempty_dst[acc]);
+      }
+    };
     uint32_t sub_ctr = 0;
     bool ok = true;
     if (g.inject_timeout) {
       ok = mbar_wait(inj_bar, 0, w, SITE_INJECT);
     }
     int lt = 0;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++lt) {
+    for (int u = unit0; u < units && ok; u += ustep, ++lt) {
       const Unit t = unit_of(u, g);
       const int acc = lt & 1;
       const uint32_t acc_par = (lt >> 1) & 1;
-      const int mrow = t.m * BM + row;                  // row within the launch's M range
+      const int slab0 = t.m * C::TILE_M + static_cast<int>(rank) * BM;   // first row of the slab
+      const int mrow = slab0 + row;                     // row within the launch's M range
       const bool row_ok = mrow < e.rows_valid;
+      const int box_row0 = slab0 + q * 32;              // first row of this warp's boxes
 
       // per-row teacher lookups, issued before waiting on the accumulator
       int hit = 0, hit_end = 0, hit_col = 1 << 30;
@@ -331,10 +398,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           s_run = s;
           m_run = m_new;
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+        release_acc(acc);
         if (row_ok) e.part[static_cast<long long>(t.n) * e.c_alloc + mrow] = make_float2(m_run, s_run);
       } else if constexpr (C::KIND == EPI_DZ) {
+        const bool box_ok = box_row0 < e.c_alloc;       // warp-uniform: inside the dZ tensor
 #pragma unroll 1
         for (int sb = 0; sb < C::BN / 64; ++sb) {
           const int c0 = sb * 64;
@@ -345,6 +412,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           reg_fence(r0);
           reg_fence(r1);
+          if (!box_ok) continue;
           float gv[64];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -369,19 +437,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, t.m * BM + q * 32);
+            tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, box_row0);
             bulk_commit();
           }
           ++sub_ctr;
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+        release_acc(acc);
       } else {
         // EPI_F32 / EPI_ACC: alpha * D -> fp32, 32-column boxes
+        const bool box_ok = box_row0 < e.rows_valid;    // warp-uniform
 #pragma unroll 1
         for (int sb = 0; sb < C::BN / 32; ++sb) {
           const int c0 = sb * 32;
-          if (t.n * C::BN + c0 >= e.cols_valid) break;   // warp-uniform
+          if (!box_ok || t.n * C::BN + c0 >= e.cols_valid) break;   // warp-uniform
           uint32_t r[32];
           tmem_ld32(tb + c0, r);
           tmem_ld_wait();
@@ -397,26 +465,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (lane == 0) {
             const void* src = sEpi + (box - smem_u32(sEpi));
             const int x = t.n * C::BN + c0;
-            const int y = e.out_row0 + t.s * e.split_rows + t.m * BM + q * 32;
+            const int y = e.out_row0 + t.s * e.split_rows + box_row0;
             if (C::KIND == EPI_ACC && !e.first) tma_reduce_add_2d(&tmO, src, x, y);
             else tma_store_2d(&tmO, src, x, y);
             bulk_commit();
           }
           ++sub_ctr;
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
+        release_acc(acc);
       }
     }
     if (C::KIND != EPI_FWD && lane == 0) bulk_wait_all();
   }
 
+  // ---------------------------------------------------------------- teardown
+  // Every TMA load issued must have landed before either CTA may exit.  A
+  // pair's loads complete on the leader's full barriers: the leader waits for
+  // the last phase of each ring slot, arming a phase that only the peer
+  // filled (it stopped early) or cancelling the peer's share of a phase that
+  // the peer never filled (the peer stopped early).
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::CTA2) cluster_sync_all(); else __syncthreads();
+  if (warp == 0 && lane == 0 && leader) {
+    const uint32_t mine = issued;
+    const uint32_t peer = C::CTA2 ? *peer_issued : issued;
+    for (int s = 0; s < C::STAGES; ++s) {
+      const uint32_t a = ring_fills(mine, s, C::STAGES);
+      const uint32_t b = ring_fills(peer, s, C::STAGES);
+      uint32_t last = a;                       // number of the phases to wait for
+      if (C::CTA2 && b == a + 1) {
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        last = b;
+      } else if (C::CTA2 && a > 0 && b + 1 == a) {
+        mbar_complete_tx(&full[s], C::STAGE_BYTES);
+      }
+      if (last > 0) mbar_wait_drain(&full[s], (last - 1) & 1u, g.timeout_ns);
+    }
+  }
+  if constexpr (C::CTA2) cluster_sync_all(); else __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    tmem_dealloc<C::NCTA>(tmem_base, C::TMEM_COLS);
   }
 }
 

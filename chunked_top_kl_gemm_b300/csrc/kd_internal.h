@@ -25,15 +25,25 @@ enum GemmVariant {
   GV_TEST_KM256 = 9,
   GV_TEST_MK256 = 10,
   GV_TEST_MM256 = 11,
+  GV_TEST_KK2 = 12,    // the four layouts on a CTA pair (256 x 256 tiles)
+  GV_TEST_KM2 = 13,
+  GV_TEST_MK2 = 14,
+  GV_TEST_MM2 = 15,
 };
 
 // Tile width of the N dimension of each variant.
 int gemm_bn(int variant);
+// M of one work unit of each variant (128, or 256 on a CTA pair).
+int gemm_tile_m(int variant);
 // Dynamic shared memory of each variant.
 int gemm_smem(int variant);
+// Work units of each variant that run at once on this device (SMs, or
+// co-resident CTA pairs).
+int gemm_width(int variant);
 
+// Launch a persistent GEMM over the units of g (grid sized by the launcher).
 cudaError_t launch_gemm(int variant, const CUtensorMap& a, const CUtensorMap& b,
-                        const CUtensorMap& o, const GemmArgs& g, const EpiArgs& e, int grid,
+                        const CUtensorMap& o, const GemmArgs& g, const EpiArgs& e,
                         cudaStream_t s);
 
 cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N, int K, int V,

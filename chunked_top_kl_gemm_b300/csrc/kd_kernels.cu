@@ -33,10 +33,13 @@
 
 namespace kd {
 
-using CfgFwd = GemmCfg<256, false, false, 4, EPI_FWD>;
-using CfgDz = GemmCfg<256, false, false, 4, EPI_DZ>;
-using CfgGradH = GemmCfg<256, true, false, 4, EPI_F32>;   // grad_hidden^T = W^T dZ^T
-using CfgGradW = GemmCfg<256, true, false, 4, EPI_ACC>;   // grad_W = dZ^T h_c
+// The loss's GEMMs run on CTA pairs (2-CTA MMA, 256 x 256 tiles): per SM
+// they pull 32 KB of operands from L2 per 64-deep k-block instead of 48 KB.
+using CfgFwd = GemmCfg<256, false, false, 7, EPI_FWD, true>;
+using CfgDz = GemmCfg<256, false, false, 6, EPI_DZ, true>;
+using CfgGradH = GemmCfg<256, true, false, 6, EPI_F32, true>;   // grad_hidden^T = W^T dZ^T
+using CfgGradW = GemmCfg<256, true, false, 6, EPI_ACC, true>;   // grad_W = dZ^T h_c
+// single-CTA forms (128 x BN tiles), kept for the GEMM-core tests
 using CfgTestKK = GemmCfg<256, false, false, 4, EPI_F32>;
 using CfgTestKM = GemmCfg<192, false, true, 4, EPI_F32>;
 using CfgTestMK = GemmCfg<192, true, false, 4, EPI_F32>;
@@ -45,10 +48,54 @@ using CfgTestKK192 = GemmCfg<192, false, false, 4, EPI_F32>;
 using CfgTestKM256 = GemmCfg<256, false, true, 4, EPI_F32>;
 using CfgTestMK256 = GemmCfg<256, true, false, 4, EPI_F32>;
 using CfgTestMM256 = GemmCfg<256, true, true, 4, EPI_F32>;
+// pair forms of the four operand layouts
+using CfgTestKK2 = GemmCfg<256, false, false, 6, EPI_F32, true>;
+using CfgTestKM2 = GemmCfg<256, false, true, 6, EPI_F32, true>;
+using CfgTestMK2 = GemmCfg<256, true, false, 6, EPI_F32, true>;
+using CfgTestMM2 = GemmCfg<256, true, true, 6, EPI_F32, true>;
+
+// Work units that can run at once: one per SM, or one per co-resident CTA
+// pair (queried once per instantiation).
+template <class C>
+static int resident_units() {
+  static int cached = 0;
+  if (cached > 0) return cached;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if constexpr (!C::CTA2) {
+    cached = sms;
+  } else {
+    if (cudaFuncSetAttribute(kd_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess) {
+      cudaGetLastError();
+      return sms / 2;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kd_gemm_kernel<C>, &cfg) != cudaSuccess ||
+        clusters <= 0) {
+      cudaGetLastError();
+      clusters = sms / 2;
+    }
+    cached = clusters;
+  }
+  return cached;
+}
 
 template <class C>
 static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                              const GemmArgs& g, const EpiArgs& e, int grid, cudaStream_t s) {
+                              const GemmArgs& g, const EpiArgs& e, cudaStream_t s) {
   static bool attr_set = false;  // per instantiation; set once per process
   if (!attr_set) {
     cudaError_t err = cudaFuncSetAttribute(kd_gemm_kernel<C>,
@@ -57,63 +104,72 @@ static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const 
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  kd_gemm_kernel<C><<<grid, NUM_THREADS, C::SMEM_BYTES, s>>>(a, b, o, g, e);
-  return cudaGetLastError();
+  const long long units = static_cast<long long>(g.m_tiles) * g.n_tiles * g.splits;
+  if (units <= 0) return cudaSuccess;
+  const int width = resident_units<C>();
+  const int grid_units = static_cast<int>(units < width ? units : width);
+  if constexpr (!C::CTA2) {
+    kd_gemm_kernel<C><<<grid_units, NUM_THREADS, C::SMEM_BYTES, s>>>(a, b, o, g, e);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * grid_units, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kd_gemm_kernel<C>, a, b, o, g, e);
+  }
 }
 
+#define KD_FOR_EACH_VARIANT(X)                                                          \
+  X(GV_FWD, CfgFwd) X(GV_DZ, CfgDz) X(GV_GRAD_H, CfgGradH) X(GV_GRAD_W, CfgGradW)         \
+  X(GV_TEST_KK, CfgTestKK) X(GV_TEST_KM, CfgTestKM) X(GV_TEST_MK, CfgTestMK)             \
+  X(GV_TEST_MM, CfgTestMM) X(GV_TEST_KK192, CfgTestKK192) X(GV_TEST_KM256, CfgTestKM256) \
+  X(GV_TEST_MK256, CfgTestMK256) X(GV_TEST_MM256, CfgTestMM256)                         \
+  X(GV_TEST_KK2, CfgTestKK2) X(GV_TEST_KM2, CfgTestKM2) X(GV_TEST_MK2, CfgTestMK2)       \
+  X(GV_TEST_MM2, CfgTestMM2)
+
 int gemm_bn(int variant) {
-  switch (variant) {
-    case GV_FWD: return CfgFwd::BN;
-    case GV_DZ: return CfgDz::BN;
-    case GV_GRAD_H: return CfgGradH::BN;
-    case GV_GRAD_W: return CfgGradW::BN;
-    case GV_TEST_KK: return CfgTestKK::BN;
-    case GV_TEST_KM: return CfgTestKM::BN;
-    case GV_TEST_MK: return CfgTestMK::BN;
-    case GV_TEST_MM: return CfgTestMM::BN;
-    case GV_TEST_KK192: return CfgTestKK192::BN;
-    case GV_TEST_KM256: return CfgTestKM256::BN;
-    case GV_TEST_MK256: return CfgTestMK256::BN;
-    case GV_TEST_MM256: return CfgTestMM256::BN;
-  }
+#define X(V, C) case V: return C::BN;
+  switch (variant) { KD_FOR_EACH_VARIANT(X) }
+#undef X
+  return 0;
+}
+
+int gemm_tile_m(int variant) {
+#define X(V, C) case V: return C::TILE_M;
+  switch (variant) { KD_FOR_EACH_VARIANT(X) }
+#undef X
   return 0;
 }
 
 int gemm_smem(int variant) {
-  switch (variant) {
-    case GV_FWD: return CfgFwd::SMEM_BYTES;
-    case GV_DZ: return CfgDz::SMEM_BYTES;
-    case GV_GRAD_H: return CfgGradH::SMEM_BYTES;
-    case GV_GRAD_W: return CfgGradW::SMEM_BYTES;
-    case GV_TEST_KK: return CfgTestKK::SMEM_BYTES;
-    case GV_TEST_KM: return CfgTestKM::SMEM_BYTES;
-    case GV_TEST_MK: return CfgTestMK::SMEM_BYTES;
-    case GV_TEST_MM: return CfgTestMM::SMEM_BYTES;
-    case GV_TEST_KK192: return CfgTestKK192::SMEM_BYTES;
-    case GV_TEST_KM256: return CfgTestKM256::SMEM_BYTES;
-    case GV_TEST_MK256: return CfgTestMK256::SMEM_BYTES;
-    case GV_TEST_MM256: return CfgTestMM256::SMEM_BYTES;
-  }
+#define X(V, C) case V: return C::SMEM_BYTES;
+  switch (variant) { KD_FOR_EACH_VARIANT(X) }
+#undef X
+  return 0;
+}
+
+int gemm_width(int variant) {
+#define X(V, C) case V: return resident_units<C>();
+  switch (variant) { KD_FOR_EACH_VARIANT(X) }
+#undef X
   return 0;
 }
 
 cudaError_t launch_gemm(int variant, const CUtensorMap& a, const CUtensorMap& b,
-                        const CUtensorMap& o, const GemmArgs& g, const EpiArgs& e, int grid,
+                        const CUtensorMap& o, const GemmArgs& g, const EpiArgs& e,
                         cudaStream_t s) {
-  switch (variant) {
-    case GV_FWD: return launch_cfg<CfgFwd>(a, b, o, g, e, grid, s);
-    case GV_DZ: return launch_cfg<CfgDz>(a, b, o, g, e, grid, s);
-    case GV_GRAD_H: return launch_cfg<CfgGradH>(a, b, o, g, e, grid, s);
-    case GV_GRAD_W: return launch_cfg<CfgGradW>(a, b, o, g, e, grid, s);
-    case GV_TEST_KK: return launch_cfg<CfgTestKK>(a, b, o, g, e, grid, s);
-    case GV_TEST_KM: return launch_cfg<CfgTestKM>(a, b, o, g, e, grid, s);
-    case GV_TEST_MK: return launch_cfg<CfgTestMK>(a, b, o, g, e, grid, s);
-    case GV_TEST_MM: return launch_cfg<CfgTestMM>(a, b, o, g, e, grid, s);
-    case GV_TEST_KK192: return launch_cfg<CfgTestKK192>(a, b, o, g, e, grid, s);
-    case GV_TEST_KM256: return launch_cfg<CfgTestKM256>(a, b, o, g, e, grid, s);
-    case GV_TEST_MK256: return launch_cfg<CfgTestMK256>(a, b, o, g, e, grid, s);
-    case GV_TEST_MM256: return launch_cfg<CfgTestMM256>(a, b, o, g, e, grid, s);
-  }
+#define X(V, C) case V: return launch_cfg<C>(a, b, o, g, e, s);
+  switch (variant) { KD_FOR_EACH_VARIANT(X) }
+#undef X
   return cudaErrorInvalidValue;
 }
 

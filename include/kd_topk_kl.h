@@ -153,12 +153,14 @@ kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* top
  *   A  bf16, [M, K] when a_mn == 0 (K contiguous) or [K, M] when a_mn != 0
  *   B  bf16, [N, K] when b_mn == 0 or [K, N] when b_mn != 0
  *   C  fp32 [M, N]
- * bn selects the tile width of the N dimension (192 or 256; 0 = the width the
- * loss uses with this layout).  M, N, K multiples of 8; all pointers device,
- * 16-byte aligned.  Synchronises `stream` before returning.
+ * pair == 0: one CTA per 128 x bn tile, bn the tile width of the N dimension
+ * (192 or 256; 0 = the default of this layout).  pair != 0: a CTA pair per
+ * 256 x 256 tile with 2-CTA MMAs, the form the loss's GEMMs use (bn 0 or
+ * 256).  M, N, K multiples of 8; all pointers device, 16-byte aligned.
+ * Synchronises `stream` before returning.
  */
 kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,
-                            int b_mn, int bn, void* stream);
+                            int b_mn, int bn, int pair, void* stream);
 
 /*
  * Per-kernel timing (diagnostics; no paper counterpart).  While enabled,
