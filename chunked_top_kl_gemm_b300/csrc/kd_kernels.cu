@@ -175,13 +175,14 @@ cudaError_t launch_gemm(int variant, const CUtensorMap& a, const CUtensorMap& b,
 
 // ------------------------------------------------------------------ prep
 // One warp per token row.  Teacher distribution over the K cached entries:
-// a_k = l_k / T, log p_k = a_k - logsumexp(a), p_k = exp(log p_k) (double).
-// Writes the row's ids sorted ascending (ties by original position) with p
-// and the original position alongside, sum_k p log p and sum_k p.  An id
+// a_k = l_k / T, log p_k = a_k - logsumexp(a), p_k = exp(log p_k), in fp32
+// (single-precision exp/log), with the row sums sum_k p log p and sum_k p
+// accumulated in double.  Writes the row's ids sorted ascending (ties by
+// original position) with p and the original position alongside.  An id
 // outside [0, V) raises DEV_ERR_INDEX.
 __global__ void __launch_bounds__(256) kd_prep_topk(const int32_t* __restrict__ idx,
                                                     const float* __restrict__ logit, long long N,
-                                                    int K, int V, double invT,
+                                                    int K, int V, float invT,
                                                     int* __restrict__ sid, float* __restrict__ sp,
                                                     int* __restrict__ perm,
                                                     double* __restrict__ ent,
@@ -193,29 +194,29 @@ __global__ void __launch_bounds__(256) kd_prep_topk(const int32_t* __restrict__ 
   int* ids = s_ids + warp * K;
   const int32_t* id_row = idx + r * K;
   const float* l_row = logit + r * K;
-  double m = -CUDART_INF;
+  float m = -CUDART_INF_F;
   bool bad = false;
   for (int k = lane; k < K; k += 32) {
     const int id = id_row[k];
     ids[k] = id;
     bad |= (id < 0) || (id >= V);
-    m = fmax(m, static_cast<double>(l_row[k]) * invT);
+    m = fmaxf(m, l_row[k] * invT);
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&st->err, DEV_ERR_INDEX);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, o));
-  double s = 0.0;
-  for (int k = lane; k < K; k += 32) s += exp(static_cast<double>(l_row[k]) * invT - m);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+  for (int k = lane; k < K; k += 32) s += expf(l_row[k] * invT - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  const double lse_t = m + log(s);
+  const float lse_t = m + logf(s);
   __syncwarp();
   double e_acc = 0.0, p_acc = 0.0;
   for (int k = lane; k < K; k += 32) {
-    const double lp = static_cast<double>(l_row[k]) * invT - lse_t;
-    const double p = exp(lp);
-    e_acc += p * lp;
-    p_acc += p;
+    const float lp = l_row[k] * invT - lse_t;
+    const float p = expf(lp);
+    e_acc += static_cast<double>(p) * static_cast<double>(lp);
+    p_acc += static_cast<double>(p);
     const int idk = ids[k];
     int rank = 0;
     for (int j = 0; j < K; ++j) {
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(256) kd_prep_topk(const int32_t* __restrict__ 
       rank += (idj < idk) || (idj == idk && j < k);
     }
     sid[r * K + rank] = idk;
-    sp[r * K + rank] = static_cast<float>(p);
+    sp[r * K + rank] = p;
     perm[r * K + rank] = k;
   }
 #pragma unroll
@@ -245,19 +246,27 @@ cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N
   const long long blocks = (N + wpb - 1) / wpb;
   const size_t smem = static_cast<size_t>(wpb) * K * 4;
   kd_prep_topk<<<static_cast<unsigned>(blocks), wpb * 32, smem, s>>>(
-      idx, logit, N, K, V, 1.0 / static_cast<double>(T), sid, sp, perm, ent, psum, st);
+      idx, logit, N, K, V, static_cast<float>(1.0 / static_cast<double>(T)), sid, sp, perm, ent,
+      psum, st);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ lse + loss fold
-// One block per 32 chunk rows (16 warps).  Lane l of every warp owns row
-// r0 + l; warp w combines the (max, sum) partials of vocab tiles w, w+16, ...
-// (log2 units, coalesced over the rows), then warp 0 merges the 16 results
-// into lse2 = log2 sum_v 2^(z_v log2e / T).  Each warp then folds two rows'
-// KL terms  sum_k p_k (log p_k - z_k/T + lse),  lse = lse2 ln 2,  with the
-// lanes striding over the K cached entries.
+// One block per 32 chunk rows (32 warps).  Lane l of every warp owns row
+// r0 + l; warp w combines the (max, sum) partials of vocab tiles w, w+32, ...
+// (log2 units, loads coalesced over the rows, four in flight per lane) in
+// fp32 relative to its running max, then warp 0 merges the 32 results in
+// double into lse2 = log2 sum_v 2^(z_v log2e / T).  Warp w then folds row
+// r0 + w's KL term  sum_k p_k (log p_k - z_k/T + lse),  lse = lse2 ln 2,
+// with the lanes striding over the K cached entries.
 constexpr int LSE_ROWS = 32;
-constexpr int LSE_WARPS = 16;
+constexpr int LSE_WARPS = 32;
+
+__device__ __forceinline__ void lse_fold(float& M, float& S, float2 v) {
+  const float m_new = fmaxf(M, v.x);
+  S = S * exp2f(M - m_new) + v.y * exp2f(v.x - m_new);
+  M = m_new;
+}
 
 __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
     const float2* __restrict__ part, int n_tiles, int c_alloc, int rows_valid, int grow0,
@@ -265,24 +274,24 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
     const double* __restrict__ ent, const double* __restrict__ psum, int K, double invT,
     float* __restrict__ lse2_out, double* __restrict__ loss_rows, float* __restrict__ dbg_lse,
     float* __restrict__ dbg_zg) {
-  __shared__ float sM[LSE_WARPS][LSE_ROWS];
-  __shared__ double sS[LSE_WARPS][LSE_ROWS];
+  __shared__ float sM[LSE_WARPS][LSE_ROWS + 1];
+  __shared__ float sS[LSE_WARPS][LSE_ROWS + 1];
   __shared__ double sLse[LSE_ROWS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * LSE_ROWS;
   const int r = r0 + lane;
-  float M = -CUDART_INF_F;
-  double S = 0.0;
+  float M = -CUDART_INF_F, S = 0.f;
   if (r < rows_valid) {
-    for (int t = warp; t < n_tiles; t += LSE_WARPS) {
-      const float2 v = part[static_cast<long long>(t) * c_alloc + r];
-      if (v.x > M) {
-        S = S * static_cast<double>(exp2f(M - v.x)) + static_cast<double>(v.y);
-        M = v.x;
-      } else {
-        S += static_cast<double>(v.y) * static_cast<double>(exp2f(v.x - M));
-      }
+    const float2* col = part + r;
+    int t = warp;
+    for (; t + 3 * LSE_WARPS < n_tiles; t += 4 * LSE_WARPS) {
+      float2 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = col[static_cast<long long>(t + i * LSE_WARPS) * c_alloc];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lse_fold(M, S, v[i]);
     }
+    for (; t < n_tiles; t += LSE_WARPS) lse_fold(M, S, col[static_cast<long long>(t) * c_alloc]);
   }
   sM[warp][lane] = M;
   sS[warp][lane] = S;
@@ -292,16 +301,15 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
     for (int w = 0; w < LSE_WARPS; ++w) Mr = fmaxf(Mr, sM[w][lane]);
     double Sr = 0.0;
     for (int w = 0; w < LSE_WARPS; ++w)
-      if (sS[w][lane] > 0.0) Sr += sS[w][lane] * static_cast<double>(exp2f(sM[w][lane] - Mr));
+      if (sS[w][lane] > 0.f)
+        Sr += static_cast<double>(sS[w][lane]) * static_cast<double>(exp2f(sM[w][lane] - Mr));
     const double lse2 = static_cast<double>(Mr) + log2(Sr);
     sLse[lane] = lse2 * 0.69314718055994530942;  // ln 2
     if (r < rows_valid) lse2_out[r] = static_cast<float>(lse2);
   }
   __syncthreads();
-  for (int i = 0; i < LSE_ROWS / LSE_WARPS; ++i) {
-    const int rr = warp * (LSE_ROWS / LSE_WARPS) + i;
-    const int row = r0 + rr;
-    if (row >= rows_valid) break;
+  const int row = r0 + warp;
+  if (row < rows_valid) {
     const long long g = static_cast<long long>(grow0) + row;
     double dot = 0.0;
     for (int j = lane; j < K; j += 32) {
@@ -312,8 +320,8 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     if (lane == 0) {
-      loss_rows[g] = ent[g] + sLse[rr] * psum[g] - dot * invT;
-      if (dbg_lse) dbg_lse[g] = static_cast<float>(sLse[rr]);
+      loss_rows[g] = ent[g] + sLse[warp] * psum[g] - dot * invT;
+      if (dbg_lse) dbg_lse[g] = static_cast<float>(sLse[warp]);
     }
   }
 }
@@ -332,36 +340,50 @@ cudaError_t launch_lse_loss(const float2* part, int n_tiles, int c_alloc, int ro
 // ------------------------------------------------------------------ split-K reduce
 // out[r][h] = alpha * sum_s part[s][h][r]  for r < rows_valid, h < H, i.e. the
 // K splits of grad_hidden^T summed in a fixed order and transposed back.
-// 32 x 32 tiles through shared memory: coalesced along r on the read side and
-// along h on the write side.
+// Tiles of 32 h x 128 r through shared memory: float4 reads along r, 128-byte
+// warp writes along h.
+constexpr int SR_H = 32, SR_R = 128;
+
 __global__ void __launch_bounds__(256) kd_split_reduce_t(const float* __restrict__ part,
                                                          int splits, long long split_stride,
                                                          int c_alloc, int rows_valid, int H,
                                                          float alpha, float* __restrict__ out) {
-  __shared__ float tile[32][33];
-  const int r0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int h = h0 + i, r = r0 + tx;
-    float a = 0.f;
-    if (h < H && r < rows_valid) {
-      const long long off = static_cast<long long>(h) * c_alloc + r;
-      a = part[off];
-      for (int sp = 1; sp < splits; ++sp) a += part[sp * split_stride + off];
+  __shared__ float tile[SR_H][SR_R + 1];
+  const int r0 = blockIdx.x * SR_R, h0 = blockIdx.y * SR_H;
+  const int t = threadIdx.x;
+  const int r4 = (t & 31) * 4;
+#pragma unroll
+  for (int i = 0; i < SR_H / 8; ++i) {
+    const int hh = (t >> 5) + 8 * i;
+    const int h = h0 + hh;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (h < H && r0 + r4 < c_alloc) {   // c_alloc is a multiple of 128
+      const long long off = static_cast<long long>(h) * c_alloc + r0 + r4;
+      a = *reinterpret_cast<const float4*>(part + off);
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 b = *reinterpret_cast<const float4*>(part + sp * split_stride + off);
+        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+      }
     }
-    tile[i][tx] = a * alpha;
+    tile[hh][r4 + 0] = a.x * alpha;
+    tile[hh][r4 + 1] = a.y * alpha;
+    tile[hh][r4 + 2] = a.z * alpha;
+    tile[hh][r4 + 3] = a.w * alpha;
   }
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int r = r0 + i, h = h0 + tx;
-    if (r < rows_valid && h < H) out[static_cast<long long>(r) * H + h] = tile[tx][i];
+  const int hh = t & 31;
+#pragma unroll 4
+  for (int j = 0; j < SR_R / 8; ++j) {
+    const int rr = (t >> 5) + 8 * j;
+    const int r = r0 + rr, h = h0 + hh;
+    if (r < rows_valid && h < H) out[static_cast<long long>(r) * H + h] = tile[hh][rr];
   }
 }
 
 cudaError_t launch_split_reduce_t(const float* part, int splits, long long split_stride,
                                   int c_alloc, int rows_valid, int H, float alpha, float* out,
                                   cudaStream_t s) {
-  dim3 grid((rows_valid + 31) / 32, (H + 31) / 32);
+  dim3 grid((rows_valid + SR_R - 1) / SR_R, (H + SR_H - 1) / SR_H);
   kd_split_reduce_t<<<grid, 256, 0, s>>>(part, splits, split_stride, c_alloc, rows_valid, H,
                                          alpha, out);
   return cudaGetLastError();
@@ -369,28 +391,42 @@ cudaError_t launch_split_reduce_t(const float* part, int splits, long long split
 
 // ------------------------------------------------------------------ chunk transpose
 // hT[h][r] = hidden[r][h] for r < rows_valid, 0 for rows_valid <= r < c_alloc
-// (bf16 copy, 32 x 32 tiles through shared memory).
+// (bf16; 64 x 64 tiles through shared memory, two elements per access).
 __global__ void __launch_bounds__(256) kd_transpose_chunk(const __nv_bfloat16* __restrict__ hid,
                                                           int rows_valid, int c_alloc, int H,
                                                           __nv_bfloat16* __restrict__ hT) {
-  __shared__ __nv_bfloat16 tile[32][34];
-  const int r0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int i = ty; i < 32; i += 8) {
-    const int r = r0 + i, h = h0 + tx;
-    tile[i][tx] = (r < rows_valid && h < H) ? hid[static_cast<long long>(r) * H + h]
-                                            : __float2bfloat16(0.f);
+  __shared__ __nv_bfloat16 tile[64][64 + 2];
+  const int r0 = blockIdx.x * 64, h0 = blockIdx.y * 64;
+  const int t = threadIdx.x;
+  const int h2 = (t & 31) * 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = (t >> 5) + 8 * i;
+    const int r = r0 + rr, h = h0 + h2;          // H is a multiple of 8: h, h+1 both valid
+    __nv_bfloat162 v = __floats2bfloat162_rn(0.f, 0.f);
+    if (r < rows_valid && h < H)
+      v = *reinterpret_cast<const __nv_bfloat162*>(hid + static_cast<long long>(r) * H + h);
+    tile[rr][h2] = v.x;
+    tile[rr][h2 + 1] = v.y;
   }
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int h = h0 + i, r = r0 + tx;
-    if (h < H && r < c_alloc) hT[static_cast<long long>(h) * c_alloc + r] = tile[tx][i];
+  const int r2 = (t & 31) * 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int hh = (t >> 5) + 8 * i;
+    const int h = h0 + hh, r = r0 + r2;          // c_alloc is a multiple of 128
+    if (h < H && r < c_alloc) {
+      __nv_bfloat162 v;
+      v.x = tile[r2][hh];
+      v.y = tile[r2 + 1][hh];
+      *reinterpret_cast<__nv_bfloat162*>(hT + static_cast<long long>(h) * c_alloc + r) = v;
+    }
   }
 }
 
 cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
                                    cudaStream_t s) {
-  dim3 grid((c_alloc + 31) / 32, (H + 31) / 32);
+  dim3 grid((c_alloc + 63) / 64, (H + 63) / 64);
   kd_transpose_chunk<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hid), rows_valid,
                                           c_alloc, H, static_cast<__nv_bfloat16*>(hT));
   return cudaGetLastError();
