@@ -34,6 +34,17 @@ Readings where the pages are silent: no T^2 factor, mean over all N tokens,
 no bias, the teacher's tail mass beyond K is dropped and p renormalised over
 the K entries, repeated ids add up (scatter-add) in dZ and give one loss term
 each.
+
+Token mask.  The pages mention sequence-packing ablations (glonce.com, body
+and "How to use it") without detail; a real training step also pads.  With
+an optional per-token mask the loss is the mean over the N_v tokens whose
+mask is set, and masked tokens contribute nothing:
+
+    loss = (1/N_v) sum_{n: mask_n} sum_k p_nk (log p_nk - log q_{n, idx_nk})
+    dZ_n = mask_n (q_n - scatter(p_n)) / (T N_v)
+
+i.e. exactly the unmasked definition applied to the valid tokens alone (a
+test checks that reading).  With N_v = 0 the loss and the gradients are 0.
 """
 from __future__ import annotations
 
@@ -89,7 +100,7 @@ def _block_terms(h_blk, W, idx_blk, logit_blk, T, N):
     """Dense logits and per-row quantities for one row block.
 
     Returns (Z, lse, zg, loss_rows, D) where D = dZ for the block, already
-    divided by T*N.
+    divided by T*N (N: the number of tokens the mean runs over).
     """
     Z = h_blk @ W.T                                   # [b, V]
     lse = student_lse(Z, T)                           # [b]
@@ -106,12 +117,14 @@ def _block_terms(h_blk, W, idx_blk, logit_blk, T, N):
 
 
 def fused_topk_kl(hidden, W, topk_idx, topk_logit, T: float,
-                  chunk_rows: int | None = None) -> dict:
+                  chunk_rows: int | None = None, mask=None) -> dict:
     """Loss and gradients of the top-K KL loss over all N tokens.
 
     ``chunk_rows`` only bounds host memory (the result does not depend on
     it; a test checks that).  Inputs may be torch tensors or arrays; all
-    arithmetic is float64.
+    arithmetic is float64.  ``mask`` (optional, [N], nonzero = the token
+    counts) restricts the mean to the valid tokens; masked tokens get zero
+    loss terms and zero gradient rows.
 
     Returns a dict with
       loss         float, mean over the N tokens
@@ -127,6 +140,8 @@ def fused_topk_kl(hidden, W, topk_idx, topk_logit, T: float,
     lg = to_f64(topk_logit)
     N, H = h.shape
     V = Wd.shape[0]
+    valid = np.ones(N, dtype=bool) if mask is None else (to_f64(mask) != 0)
+    n_valid = int(valid.sum())
     if chunk_rows is None:
         chunk_rows = max(1, min(N, (1 << 28) // max(V, 1)))
     out_lse = np.empty(N)
@@ -137,14 +152,18 @@ def fused_topk_kl(hidden, W, topk_idx, topk_logit, T: float,
     for r0 in range(0, N, chunk_rows):
         r1 = min(N, r0 + chunk_rows)
         _, lse, zg, lrow, D = _block_terms(h[r0:r1], Wd, idx[r0:r1],
-                                           lg[r0:r1], T, N)
+                                           lg[r0:r1], T, max(n_valid, 1))
+        keep = valid[r0:r1]
+        lrow = np.where(keep, lrow, 0.0)
+        D = D * keep[:, None]
         out_lse[r0:r1] = lse
         out_zg[r0:r1] = zg
         out_loss_rows[r0:r1] = lrow
         gh[r0:r1] = D @ Wd
         gW += D.T @ h[r0:r1]
     return {
-        "loss": float(out_loss_rows.sum() / N),
+        "loss": float(out_loss_rows.sum() / n_valid) if n_valid else 0.0,
+        "n_valid": n_valid,
         "loss_rows": out_loss_rows,
         "lse": out_lse,
         "zg": out_zg,

@@ -192,3 +192,78 @@ ALL_PINS = (
     pin_library_kl, pin_self_distillation, pin_two_token_vocab,
     pin_nonnegative, pin_invariants,
 )
+
+
+# ---------------------------------------------------------------- token mask
+# Pins of the masked loss take ``impl_m(hidden, W, idx, logit, T, mask)``.
+#
+# * ``pin_mask_subset``  -- the masked loss is the unmasked loss of the valid
+#   tokens alone (the definition of "mean over the valid tokens"): the same
+#   loss and grad_W, the same grad_hidden rows, zero rows for masked tokens;
+#   an all-ones mask changes nothing; an all-zero mask gives zeros.
+# * ``pin_mask_fd``      -- calculus: the masked gradients are the derivatives
+#   of the masked loss (central differences, float64).
+# * ``pin_mask_torch``   -- library reduction: torch log_softmax / kl_div with
+#   the mask applied per token and autograd, float64.
+
+def _mask_case(seed=7, N=8, H=5, V=26, K=4):
+    h, W, idx, lg = small_case(seed, N=N, H=H, V=V, K=K)
+    mask = (_rng(seed + 50).random(N) < 0.6).astype(np.uint8)
+    mask[0], mask[1] = 1, 0
+    return h, W, idx, lg, mask
+
+
+def pin_mask_subset(impl_m, T):
+    h, W, idx, lg, mask = _mask_case()
+    out = impl_m(h, W, idx, lg, T, mask)
+    keep = mask != 0
+    sub = impl_m(h[keep], W, idx[keep], lg[keep], T, np.ones(int(keep.sum())))
+    assert abs(out["loss"] - sub["loss"]) <= 1e-12 * max(1.0, abs(sub["loss"]))
+    assert np.abs(out["grad_W"] - sub["grad_W"]).max() <= 1e-14
+    assert np.abs(out["grad_hidden"][keep] - sub["grad_hidden"]).max() <= 1e-14
+    assert np.abs(out["grad_hidden"][~keep]).max() == 0.0
+    full = impl_m(h, W, idx, lg, T, np.ones(len(mask)))
+    plain = impl_m(h, W, idx, lg, T, None)
+    assert full["loss"] == plain["loss"]
+    assert np.array_equal(full["grad_W"], plain["grad_W"])
+    none = impl_m(h, W, idx, lg, T, np.zeros(len(mask)))
+    assert none["loss"] == 0.0
+    assert np.abs(none["grad_W"]).max() == 0.0 and np.abs(none["grad_hidden"]).max() == 0.0
+
+
+def pin_mask_fd(impl_m, T, eps=1e-6, tol=1e-6):
+    h, W, idx, lg, mask = _mask_case(N=6, H=4, V=15, K=3)
+    out = impl_m(h, W, idx, lg, T, mask)
+    for name, X, G in (("hidden", h, out["grad_hidden"]), ("W", W, out["grad_W"])):
+        fd = np.empty_like(X)
+        for i in np.ndindex(X.shape):
+            Xp = X.copy(); Xp[i] += eps
+            Xm = X.copy(); Xm[i] -= eps
+            args_p = (Xp, W) if name == "hidden" else (h, Xp)
+            args_m = (Xm, W) if name == "hidden" else (h, Xm)
+            fd[i] = (impl_m(*args_p, idx, lg, T, mask)["loss"]
+                     - impl_m(*args_m, idx, lg, T, mask)["loss"]) / (2 * eps)
+        err = np.abs(fd - G).max() / max(np.abs(fd).max(), 1e-300)
+        assert err <= tol, f"masked FD mismatch on {name}: rel {err:.3e}"
+
+
+def pin_mask_torch(impl_m, T):
+    h, W, idx, lg, mask = _mask_case(seed=9, N=10, H=6, V=21, K=5)
+    out = impl_m(h, W, idx, lg, T, mask)
+    ht = torch.tensor(h, dtype=torch.float64, requires_grad=True)
+    Wt = torch.tensor(W, dtype=torch.float64, requires_grad=True)
+    logq = torch.log_softmax((ht @ Wt.T) / T, dim=1).gather(
+        1, torch.tensor(np.asarray(idx), dtype=torch.int64))
+    lp = torch.log_softmax(torch.tensor(lg, dtype=torch.float64) / T, dim=1)
+    per_tok = torch.nn.functional.kl_div(logq, lp, log_target=True,
+                                         reduction="none").sum(dim=1)
+    m = torch.tensor(mask, dtype=torch.float64)
+    loss = (per_tok * m).sum() / m.sum()
+    loss.backward()
+    lv = float(loss.detach())
+    assert abs(out["loss"] - lv) <= 1e-12 * max(1.0, abs(lv))
+    for got, want in ((out["grad_hidden"], ht.grad.numpy()), (out["grad_W"], Wt.grad.numpy())):
+        assert np.abs(got - want).max() <= 1e-12 * max(np.abs(want).max(), 1e-300)
+
+
+MASK_PINS = (pin_mask_subset, pin_mask_fd, pin_mask_torch)

@@ -78,3 +78,13 @@ def test_tiny_config_loss_is_sane(name):
     assert 0 < out["loss"] < np.log(cfg.V) + 1
     assert np.isfinite(out["grad_hidden"]).all() and np.isfinite(out["grad_W"]).all()
     assert np.abs(out["grad_W"].sum(axis=0)).max() < 1e-12
+
+
+def impl_m(h, W, idx, lg, T, mask):
+    return oracle.fused_topk_kl(h, W, idx, lg, T, mask=mask)
+
+
+@pytest.mark.parametrize("T", [1.0, 2.5])
+@pytest.mark.parametrize("pin", pins.MASK_PINS, ids=lambda f: f.__name__)
+def test_mask_pin(pin, T):
+    pin(impl_m, T)

@@ -66,6 +66,40 @@ def test_some_pin_rejects_mutant(mut, monkeypatch):
     assert caught, f"no pin rejects mutant {mut}"
 
 
+def test_mask_mean_over_all_tokens_is_rejected(monkeypatch):
+    # planted mistake: the masked mean divides by N instead of the number of
+    # valid tokens (and scales dZ the same way)
+    real = kl_topk.fused_topk_kl
+
+    def wrong(h, W, idx, lg, T, chunk_rows=None, mask=None):
+        out = real(h, W, idx, lg, T, chunk_rows=chunk_rows, mask=mask)
+        n = np.asarray(h).shape[0]
+        if mask is not None and out["n_valid"]:
+            f = out["n_valid"] / n
+            out = dict(out, loss=out["loss"] * f, grad_hidden=out["grad_hidden"] * f,
+                       grad_W=out["grad_W"] * f)
+        return out
+
+    caught = []
+    for pin in pins.MASK_PINS:
+        try:
+            pin(lambda h, W, i, l, T, m: wrong(h, W, i, l, T, mask=m), 1.0)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught
+
+
+def test_mask_dropped_is_rejected():
+    # planted mistake: the mask is ignored
+    caught = []
+    for pin in pins.MASK_PINS:
+        try:
+            pin(lambda h, W, i, l, T, m: oracle.fused_topk_kl(h, W, i, l, T), 1.0)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught
+
+
 def test_unmutated_oracle_passes_every_pin():
     for pin in pins.ALL_PINS:
         pin(lambda h, W, i, l, T: oracle.fused_topk_kl(h, W, i, l, T), 1.0)
