@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
     L.kd_topk_kl_fwd_bwd.restype = i32
     L.kd_topk_kl_fwd_bwd_ex.argtypes = common + [vp, sz, vp]
     L.kd_topk_kl_fwd_bwd_ex.restype = i32
+    L.kd_topk_kl_fwd_bwd_masked.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
+                                             i32, vp, vp, vp, vp, sz, vp]
+    L.kd_topk_kl_fwd_bwd_masked.restype = i32
     L.kd_topk_kl_debug.argtypes = common + [vp, sz, vp, ctypes.POINTER(_DebugOpts)]
     L.kd_topk_kl_debug.restype = i32
     L.kd_topk_kl_workspace_size.argtypes = [i64, i32, i32, i32, i32]
@@ -178,6 +181,28 @@ def kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
     return float(loss.value)
 
 
+def kd_topk_kl_fwd_bwd_masked(hidden, W, topk_idx, topk_logit, token_mask, T: float,
+                              chunk: int, grad_hidden, grad_W, workspace, accumulate=False,
+                              stream=None) -> float:
+    """Per-token mask (uint8/bool [N] CUDA tensor or None) and accumulate flag."""
+    import torch
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    if token_mask is not None:
+        if token_mask.dtype == torch.bool:
+            token_mask = token_mask.view(torch.uint8)
+        if token_mask.dtype != torch.uint8 or token_mask.shape != (N,) or not token_mask.is_cuda \
+                or not token_mask.is_contiguous():
+            raise ValueError("token_mask must be a contiguous uint8/bool CUDA tensor of shape [N]")
+    loss = ctypes.c_float(0.0)
+    st = lib().kd_topk_kl_fwd_bwd_masked(
+        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
+        float(T), int(chunk), 1 if accumulate else 0, ctypes.addressof(loss), _ptr(grad_hidden),
+        _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd_masked")
+    return float(loss.value)
+
+
 def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad_hidden,
                      grad_W, workspace, *, lse=None, zg=None, found_idx=None, loss_rows=None,
                      timeout_ns: int = 0, inject_timeout: bool = False, stream=None) -> float:
@@ -230,23 +255,32 @@ def alloc_workspace(N: int, H: int, V: int, K: int, chunk: int, device=None):
 
 
 def fwd_bwd(hidden, W, topk_idx, topk_logit, T: float = 1.0, chunk: int = 2048, *,
-            workspace=None, grad_hidden=None, grad_W=None, stream=None):
+            workspace=None, grad_hidden=None, grad_W=None, stream=None, token_mask=None,
+            accumulate: bool = False):
     """Loss (float) and fp32 grad_hidden [N,H], grad_W [V,H] of the top-K KL.
 
     Outputs and the workspace are allocated with torch on hidden's device
-    unless given.
+    unless given.  ``token_mask`` restricts the mean to the valid tokens;
+    ``accumulate`` adds into the given gradient tensors.
     """
     import torch
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     dev = hidden.device
+    if accumulate and (grad_hidden is None or grad_W is None):
+        raise ValueError("accumulate=True needs grad_hidden and grad_W to add into")
     if grad_hidden is None:
         grad_hidden = torch.empty((N, H), dtype=torch.float32, device=dev)
     if grad_W is None:
         grad_W = torch.empty((V, H), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = alloc_workspace(N, H, V, K, chunk, device=dev)
-    loss = kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T, chunk, grad_hidden,
-                                 grad_W, workspace, stream=stream)
+    if token_mask is None and not accumulate:
+        loss = kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T, chunk, grad_hidden,
+                                     grad_W, workspace, stream=stream)
+    else:
+        loss = kd_topk_kl_fwd_bwd_masked(hidden, W, topk_idx, topk_logit, token_mask, T, chunk,
+                                         grad_hidden, grad_W, workspace, accumulate=accumulate,
+                                         stream=stream)
     return loss, grad_hidden, grad_W
 
 

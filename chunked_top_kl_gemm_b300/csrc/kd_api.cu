@@ -242,11 +242,16 @@ kd_status validate(const void* hidden, const void* W, const int32_t* idx, const 
   return KD_OK;
 }
 
+// The whole path on stream s.  mask (optional, device [N]): nonzero = the
+// token counts; the mean runs over the valid tokens and masked tokens get
+// zero gradient rows.  accumulate: add into grad_hidden / grad_W.
 kd_status run(const void* hidden, const void* W, const int32_t* idx, const float* logit,
               long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
-              float* gW, void* ws, size_t ws_bytes, cudaStream_t s, const kd_debug_opts* opts) {
+              float* gW, void* ws, size_t ws_bytes, cudaStream_t s, const kd_debug_opts* opts,
+              const uint8_t* mask = nullptr, int accumulate = 0) {
   kd_status st = validate(hidden, W, idx, logit, N, H, V, K, T, chunk, loss, gh, gW);
   if (st != KD_OK) return st;
+  if (mask && !is_device_ptr(mask)) return KD_ERR_INVALID_ARG;
   const Plan p = make_plan(N, H, V, K, chunk, device_sms());
   if (!ws || ws_bytes < p.total) return KD_ERR_OOM;
   prof().used = 0;
@@ -297,6 +302,12 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   const float alpha = static_cast<float>(1.0 / (static_cast<double>(T) * static_cast<double>(N)));
 
   KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
+  // masked calls: n_valid and the gradient scale 1/(T n_valid) on the device
+  const float* alpha_dev = nullptr;
+  if (mask) {
+    KD_CUDA(kd::launch_mask_count(mask, N, T, dst, s));
+    alpha_dev = &dst->alpha;
+  }
   { ProfScope ps_(PK_PREP, s); KD_CUDA(kd::launch_prep_topk(idx, logit, N, K, V, T, sid, sp, perm, ent, psum, dst, s)); }
 
   for (int j = 0; j < p.n_chunks; ++j) {
@@ -314,9 +325,10 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     e.K = K; e.grow0 = row0; e.c_alloc = p.chunk;
     e.sid = sid; e.sp = sp; e.perm = perm; e.part = part; e.zg = zg; e.lse2 = lse2;
     e.dbg_found = dbg_found;
+    e.mask = mask;
     { ProfScope ps_(PK_FWD, s); KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e, s)); }
 
-    { ProfScope ps_(PK_LSE, s); KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, lse2,
+    { ProfScope ps_(PK_LSE, s); KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, mask, lse2,
                                 loss_rows, dbg_lse, dbg_zg, s)); }
 
     g.inject_timeout = 0;
@@ -335,7 +347,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     e2.split_rows = p.hp;
     { ProfScope ps_(PK_GRAD_H, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_H, tm_w_mn, tm_dz_k256, tm_k4_st, g2, e2, s)); }
     { ProfScope ps_(PK_SPLIT_RED, s); KD_CUDA(kd::launch_split_reduce_t(k4, p.splits,
-                                    static_cast<long long>(p.hp) * p.chunk, p.chunk, cj, H, alpha,
+                                    static_cast<long long>(p.hp) * p.chunk, p.chunk, cj, H, alpha, alpha_dev, accumulate,
                                     gh + static_cast<long long>(row0) * H, s)); }
 
     // grad_W += dZ^T h_c   (B operand: h_c^T, K-major)
@@ -349,7 +361,8 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     g3.timeout_ns = timeout; g3.status = dst;
     kd::EpiArgs e3{};
     e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
-    e3.first = (j == 0);
+    e3.alpha_dev = alpha_dev;
+    e3.first = (j == 0) && !accumulate;
     { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_ht_k, tm_gw, g3, e3, s)); }
   }
   { ProfScope ps_(PK_FINAL, s); KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s)); }
@@ -363,7 +376,8 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   prof_collect();
   if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
   if (hs.err & kd::DEV_ERR_INDEX) return KD_ERR_INDEX;
-  *loss = static_cast<float>(hs.loss_sum / static_cast<double>(N));
+  const long long n_mean = mask ? hs.n_valid : N;
+  *loss = n_mean > 0 ? static_cast<float>(hs.loss_sum / static_cast<double>(n_mean)) : 0.f;
   return KD_OK;
 }
 
@@ -382,6 +396,17 @@ kd_status kd_topk_kl_fwd_bwd_ex(const void* hidden, const void* W, const int32_t
                                 void* workspace, size_t workspace_bytes, void* stream) {
   return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
              workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+kd_status kd_topk_kl_fwd_bwd_masked(const void* hidden, const void* W, const int32_t* topk_idx,
+                                    const float* topk_logit, const uint8_t* token_mask,
+                                    int64_t N, int H, int V, int K, float T, int chunk,
+                                    int accumulate, float* loss, float* grad_hidden,
+                                    float* grad_W, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
+             workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, token_mask,
+             accumulate);
 }
 
 kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* topk_idx,

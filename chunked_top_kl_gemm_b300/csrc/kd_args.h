@@ -42,6 +42,8 @@ struct EpiArgs {
   float* zg;             // EPI_FWD: [c_alloc][K] z at the sorted ids
   const float* lse2;     // EPI_DZ: [c_alloc] log2-sum-exp2 of z*log2e/T
   int* dbg_found;        // EPI_FWD: optional [N][K] column at which id k was found
+  const uint8_t* mask;   // EPI_DZ: optional [N] token mask (0 = the token's dZ row is 0)
+  const float* alpha_dev;  // EPI_ACC: optional device scale, read instead of alpha
 };
 
 }  // namespace kd

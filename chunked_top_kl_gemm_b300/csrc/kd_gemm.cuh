@@ -356,6 +356,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if constexpr (C::KIND == EPI_DZ) lse2 = __ldg(e.lse2 + mrow);
         }
       }
+      // EPI_DZ: a masked token's dZ row is zero
+      bool row_live = row_ok;
+      if constexpr (C::KIND == EPI_DZ) {
+        if (row_ok && e.mask && __ldg(e.mask + e.grow0 + mrow) == 0) {
+          row_live = false;
+          hit_col = 1 << 30;
+        }
+      }
 
       bool got = mbar_wait(&tfull[acc], acc_par, w, SITE_EPI);
       got = __all_sync(0xffffffffu, got);
@@ -416,8 +424,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float gv[64];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            gv[j] = row_ok ? ex2_approx(fmaf(__uint_as_float(r0[j]), e.scale2, -lse2)) : 0.f;
-            gv[32 + j] = row_ok ? ex2_approx(fmaf(__uint_as_float(r1[j]), e.scale2, -lse2)) : 0.f;
+            gv[j] = row_live ? ex2_approx(fmaf(__uint_as_float(r0[j]), e.scale2, -lse2)) : 0.f;
+            gv[32 + j] = row_live ? ex2_approx(fmaf(__uint_as_float(r1[j]), e.scale2, -lse2)) : 0.f;
           }
           while (hit_col < c0 + 64) {
             const float p = __ldg(e.sp + static_cast<long long>(e.grow0 + mrow) * e.K + hit);
@@ -446,6 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         // EPI_F32 / EPI_ACC: alpha * D -> fp32, 32-column boxes
         const bool box_ok = box_row0 < e.rows_valid;    // warp-uniform
+        const float alpha = e.alpha_dev ? __ldg(e.alpha_dev) : e.alpha;
 #pragma unroll 1
         for (int sb = 0; sb < C::BN / 32; ++sb) {
           const int c0 = sb * 32;
@@ -455,7 +464,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           reg_fence(r);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * e.alpha);
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
           const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();

@@ -52,12 +52,16 @@ cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N
 
 cudaError_t launch_lse_loss(const float2* part, int n_tiles, int c_alloc, int rows_valid, int grow0,
                             const float* zg, const float* sp, const int* perm, const double* ent,
-                            const double* psum, int K, float T, float* lse2, double* loss_rows,
-                            float* dbg_lse, float* dbg_zg, cudaStream_t s);
+                            const double* psum, int K, float T, const uint8_t* mask, float* lse2,
+                            double* loss_rows, float* dbg_lse, float* dbg_zg, cudaStream_t s);
 
 cudaError_t launch_split_reduce_t(const float* part, int splits, long long split_stride,
-                                  int c_alloc, int rows_valid, int H, float alpha, float* out,
+                                  int c_alloc, int rows_valid, int H, float alpha,
+                                  const float* alpha_dev, int accumulate, float* out,
                                   cudaStream_t s);
+
+cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStatus* st,
+                              cudaStream_t s);
 
 cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
                                    cudaStream_t s);

@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
     const float2* __restrict__ part, int n_tiles, int c_alloc, int rows_valid, int grow0,
     const float* __restrict__ zg, const float* __restrict__ sp, const int* __restrict__ perm,
     const double* __restrict__ ent, const double* __restrict__ psum, int K, double invT,
-    float* __restrict__ lse2_out, double* __restrict__ loss_rows, float* __restrict__ dbg_lse,
-    float* __restrict__ dbg_zg) {
+    const uint8_t* __restrict__ mask, float* __restrict__ lse2_out,
+    double* __restrict__ loss_rows, float* __restrict__ dbg_lse, float* __restrict__ dbg_zg) {
   __shared__ float sM[LSE_WARPS][LSE_ROWS + 1];
   __shared__ float sS[LSE_WARPS][LSE_ROWS + 1];
   __shared__ double sLse[LSE_ROWS];
@@ -320,7 +320,8 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     if (lane == 0) {
-      loss_rows[g] = ent[g] + sLse[warp] * psum[g] - dot * invT;
+      const bool live = !mask || mask[g] != 0;
+      loss_rows[g] = live ? ent[g] + sLse[warp] * psum[g] - dot * invT : 0.0;
       if (dbg_lse) dbg_lse[g] = static_cast<float>(sLse[warp]);
     }
   }
@@ -328,18 +329,20 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
 
 cudaError_t launch_lse_loss(const float2* part, int n_tiles, int c_alloc, int rows_valid, int grow0,
                             const float* zg, const float* sp, const int* perm, const double* ent,
-                            const double* psum, int K, float T, float* lse2, double* loss_rows,
-                            float* dbg_lse, float* dbg_zg, cudaStream_t s) {
+                            const double* psum, int K, float T, const uint8_t* mask, float* lse2,
+                            double* loss_rows, float* dbg_lse, float* dbg_zg, cudaStream_t s) {
   const int blocks = (rows_valid + LSE_ROWS - 1) / LSE_ROWS;
   kd_lse_loss<<<blocks, LSE_WARPS * 32, 0, s>>>(part, n_tiles, c_alloc, rows_valid, grow0, zg, sp,
                                                 perm, ent, psum, K, 1.0 / static_cast<double>(T),
-                                                lse2, loss_rows, dbg_lse, dbg_zg);
+                                                mask, lse2, loss_rows, dbg_lse, dbg_zg);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ split-K reduce
 // out[r][h] = alpha * sum_s part[s][h][r]  for r < rows_valid, h < H, i.e. the
-// K splits of grad_hidden^T summed in a fixed order and transposed back.
+// K splits of grad_hidden^T summed in a fixed order and transposed back
+// (added to out instead when `accumulate`; alpha read from alpha_dev when
+// that is given).
 // Tiles of 32 h x 128 r through shared memory: float4 reads along r, 128-byte
 // warp writes along h.
 constexpr int SR_H = 32, SR_R = 128;
@@ -347,8 +350,11 @@ constexpr int SR_H = 32, SR_R = 128;
 __global__ void __launch_bounds__(256) kd_split_reduce_t(const float* __restrict__ part,
                                                          int splits, long long split_stride,
                                                          int c_alloc, int rows_valid, int H,
-                                                         float alpha, float* __restrict__ out) {
+                                                         float alpha_host,
+                                                         const float* __restrict__ alpha_dev,
+                                                         int accumulate, float* __restrict__ out) {
   __shared__ float tile[SR_H][SR_R + 1];
+  const float alpha = alpha_dev ? *alpha_dev : alpha_host;
   const int r0 = blockIdx.x * SR_R, h0 = blockIdx.y * SR_H;
   const int t = threadIdx.x;
   const int r4 = (t & 31) * 4;
@@ -376,16 +382,20 @@ __global__ void __launch_bounds__(256) kd_split_reduce_t(const float* __restrict
   for (int j = 0; j < SR_R / 8; ++j) {
     const int rr = (t >> 5) + 8 * j;
     const int r = r0 + rr, h = h0 + hh;
-    if (r < rows_valid && h < H) out[static_cast<long long>(r) * H + h] = tile[hh][rr];
+    if (r < rows_valid && h < H) {
+      float* o = out + static_cast<long long>(r) * H + h;
+      *o = accumulate ? *o + tile[hh][rr] : tile[hh][rr];
+    }
   }
 }
 
 cudaError_t launch_split_reduce_t(const float* part, int splits, long long split_stride,
-                                  int c_alloc, int rows_valid, int H, float alpha, float* out,
+                                  int c_alloc, int rows_valid, int H, float alpha,
+                                  const float* alpha_dev, int accumulate, float* out,
                                   cudaStream_t s) {
   dim3 grid((rows_valid + SR_R - 1) / SR_R, (H + SR_H - 1) / SR_H);
   kd_split_reduce_t<<<grid, 256, 0, s>>>(part, splits, split_stride, c_alloc, rows_valid, H,
-                                         alpha, out);
+                                         alpha, alpha_dev, accumulate, out);
   return cudaGetLastError();
 }
 
@@ -429,6 +439,35 @@ cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc,
   dim3 grid((c_alloc + 63) / 64, (H + 63) / 64);
   kd_transpose_chunk<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hid), rows_valid,
                                           c_alloc, H, static_cast<__nv_bfloat16*>(hT));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ token mask
+// n_valid = number of tokens whose mask byte is nonzero; alpha = 1/(T n_valid)
+// (0 when no token is valid), the gradient scale of a masked call.
+__global__ void __launch_bounds__(1024) kd_mask_count(const uint8_t* __restrict__ mask,
+                                                      long long N, double T, DevStatus* st) {
+  __shared__ long long red[32];
+  long long c = 0;
+  for (long long i = threadIdx.x; i < N; i += 1024) c += mask[i] != 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    c = red[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (threadIdx.x == 0) {
+      st->n_valid = c;
+      st->alpha = c > 0 ? static_cast<float>(1.0 / (T * static_cast<double>(c))) : 0.f;
+    }
+  }
+}
+
+cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStatus* st,
+                              cudaStream_t s) {
+  kd_mask_count<<<1, 1024, 0, s>>>(mask, N, static_cast<double>(T), st);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,9 @@ struct DevStatus {
   double loss_sum;   // sum over tokens of the per-token KL term
   int err;           // OR of DEV_ERR_* bits
   int where;         // first failing wait site (debug)
+  long long n_valid; // tokens whose mask is set (masked calls)
+  float alpha;       // 1 / (T n_valid), or 0 when no token is valid (masked calls)
+  int pad_;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -116,6 +116,29 @@ kd_status kd_topk_kl_fwd_bwd_ex(const void* hidden, const void* W, const int32_t
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kd_topk_kl_fwd_bwd_ex with a per-token mask and an accumulate flag, for a
+ * training step with padding or sequence packing (the pages mention packing
+ * ablations only: glonce.com, body and "How to use it").
+ *
+ *   token_mask  uint8 [N] (device) or NULL.  Nonzero = the token counts.  The
+ *               loss is the mean over the N_v valid tokens,
+ *                 loss = (1/N_v) sum_{n valid} sum_k p_nk (log p_nk - log q_{n,idx_nk}),
+ *               a masked token contributes no loss and zero gradient rows,
+ *               and dZ is scaled by 1/(T N_v).  N_v = 0 gives loss 0 and zero
+ *               gradients.  NULL = every token counts (same as _ex).
+ *               Masked tokens' ids are still range-checked.
+ *   accumulate  nonzero: grad_hidden += and grad_W += the call's gradients
+ *               (both must hold finite values on entry); 0: overwrite.
+ * Every other argument as for kd_topk_kl_fwd_bwd_ex.
+ */
+kd_status kd_topk_kl_fwd_bwd_masked(const void* hidden, const void* W, const int32_t* topk_idx,
+                                    const float* topk_logit, const uint8_t* token_mask,
+                                    int64_t N, int H, int V, int K, float T, int chunk,
+                                    int accumulate, float* loss, float* grad_hidden,
+                                    float* grad_W, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
  * Test and diagnosis options for kd_topk_kl_debug.  Each output pointer may
  * be NULL (not written).
  *   lse        fp32 [N]    logsumexp_v(z_n / T) (device)
