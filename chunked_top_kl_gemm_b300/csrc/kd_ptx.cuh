@@ -113,15 +113,15 @@ struct WaitCtx {
   uint64_t timeout_ns;
 };
 
-// Wait until the phase with parity `parity` of `bar` has completed.  Returns
-// false (and raises the abort word and the device error) when the limit
-// runs out or another role of the CTA has aborted.
-template <bool CLUSTER = false>
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w,
-                                       int site) {
+// Slow path of mbar_wait: poll until the phase with parity `parity` of `bar`
+// has completed.  Returns false (and raises the abort word and the device
+// error) when the limit runs out or another role of the CTA has aborted.
+// Out of line, so the hot loops carry only the inline first poll.
+template <bool CLUSTER>
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   const WaitCtx& w, int site) {
   const uint32_t a = smem_u32(bar);
   auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
-  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (poll()) return true;
@@ -134,6 +134,18 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, co
       }
     }
   }
+}
+
+// Wait until the phase with parity `parity` of `bar` has completed (bounded;
+// see mbar_wait_slow).  The first poll is inline: in a balanced pipeline
+// the phase has usually completed already, and a function call per k-block
+// on the MMA and producer threads costs tensor-pipe cycles.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w,
+                                          int site) {
+  const uint32_t a = smem_u32(bar);
+  if (CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+  return mbar_wait_slow<CLUSTER>(bar, parity, w, site);
 }
 
 // ---------------------------------------------------------------- TMA
