@@ -274,6 +274,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int lt = 0;
       bool ok = true;
+      // Shared-memory descriptors of ring slot 0; slot s is slot 0 advanced by
+      // s stage sizes in the 16-byte address field (smem < 256 KB: no carry).
+      const uint64_t a_desc0 = C::A_MN ? sdesc_sw128(smem_u32(sA), 8192, 1024)
+                                       : sdesc_sw128(smem_u32(sA), 16, 1024);
+      const uint64_t b_desc0 = C::B_MN ? sdesc_sw128(smem_u32(sB), 8192, 1024)
+                                       : sdesc_sw128(smem_u32(sB), 16, 1024);
+      constexpr uint32_t A_STEP = C::A_BYTES >> 4, B_STEP = C::B_BYTES >> 4;
+      constexpr uint32_t A_KK = C::A_MN ? (2048 >> 4) : (32 >> 4);   // one UMMA_K slice
+      constexpr uint32_t B_KK = C::B_MN ? (2048 >> 4) : (32 >> 4);
+      uint64_t a_desc = a_desc0, b_desc = b_desc0;
       for (int u = unit0; u < units && ok; u += ustep, ++lt) {
         const Unit t = unit_of(u, g);
         const int acc = lt & 1;
@@ -284,22 +294,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // a ragged last N tile multiplies only its valid columns
         const int nn = tile_cols(t.n);
         const uint32_t idesc_t = idesc_bf16(C::TILE_M, nn, C::A_MN, C::B_MN);
+        uint32_t first = 0;   // the unit's first MMA overwrites the accumulator
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, w, SITE_MMA_FULL)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a = smem_u32(sA + stage * C::A_BYTES);
-          const uint32_t b = smem_u32(sB + stage * C::B_BYTES);
+          tc_mma_bf16<C::NCTA>(d, a_desc, b_desc, idesc_t, first);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t ad = C::A_MN ? sdesc_sw128(a + kk * 2048, 8192, 1024)
-                                        : sdesc_sw128(a + kk * 32, 16, 1024);
-            const uint64_t bd = C::B_MN ? sdesc_sw128(b + kk * 2048, 8192, 1024)
-                                        : sdesc_sw128(b + kk * 32, 16, 1024);
-            tc_mma_bf16<C::NCTA>(d, ad, bd, idesc_t, (kb > t.kb0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 1; kk < BK / UMMA_K; ++kk)
+            tc_mma_bf16_acc<C::NCTA>(d, a_desc + kk * A_KK, b_desc + kk * B_KK, idesc_t);
+          first = 1;
           if constexpr (C::CTA2) tc_commit_pair(&empty[stage]);
           else tc_commit<1>(&empty[stage]);
-          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+            a_desc = a_desc0;
+            b_desc = b_desc0;
+          } else {
+            a_desc += A_STEP;
+            b_desc += B_STEP;
+          }
         }
         if (ok) {
           if constexpr (C::CTA2) tc_commit_pair(&tfull[acc]);

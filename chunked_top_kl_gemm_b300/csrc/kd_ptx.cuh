@@ -266,6 +266,20 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The same, always accumulating into D (no predicate to set up).
+template <int NCTA>
+__device__ __forceinline__ void tc_mma_bf16_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc) {
+  if constexpr (NCTA == 1)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc)
+                 : "memory");
+}
+
 // Arrive once on `bar` (this CTA's) when every tcgen05 operation issued so
 // far by this thread has completed.
 template <int NCTA>
