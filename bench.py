@@ -247,13 +247,20 @@ def run_gpu(args):
     h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
     gh = torch.empty((N, H), dtype=torch.float32, device=dev)
     gW = torch.empty((V, H), dtype=torch.float32, device=dev)
-    ws = kd.alloc_workspace(N, H, V, K, chunk, device=dev)
+    flags = kd.KD_FLAG_STORE_LOGITS if args.store_logits else 0
+    ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, flags),
+                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
     del inp
 
-    def step():
-        return kd.kd_topk_kl_fwd_bwd_ex(h, W, idx, lg, T, chunk, gh, gW, ws, stream=stream)
+    if args.store_logits:
+        def step():
+            return kd.kd_topk_kl_fwd_bwd_flags(h, W, idx, lg, None, T, chunk, flags, gh, gW, ws,
+                                               stream=stream)
+    else:
+        def step():
+            return kd.kd_topk_kl_fwd_bwd_ex(h, W, idx, lg, T, chunk, gh, gW, ws, stream=stream)
 
     for _ in range(max(args.warmup, 3) if not args.allow_short_warmup else args.warmup):
         loss = step()
@@ -281,7 +288,9 @@ def run_gpu(args):
     t_dev = e0.elapsed_time(e1) / 1e3
     t_max = dist_max(t_dev, dev)
     value = throughput(N, args.steps, world, t_max)
-    tflops = cfg.flops * args.steps / t_max / 1e12
+    # the recompute path does four GEMMs of 2NHV; storing the logits skips one
+    flops_step = cfg.flops * (0.75 if args.store_logits else 1.0)
+    tflops = flops_step * args.steps / t_max / 1e12
 
     # end to end: pinned host inputs copied in every step, loss read back
     h_host = h.cpu().pin_memory()
@@ -336,6 +345,8 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {"workload": cfg.name, "N": N, "H": H, "V": V, "K": K, "T": T,
                    "chunk": chunk, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "backward": "stored fp32 logits (6NHV)" if args.store_logits
+                               else "recompute (8NHV)",
                    "l2": "inputs larger than L2 (W is 1.16 GB and is streamed every GEMM)"},
         "tflops": tflops,
         "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
@@ -374,6 +385,8 @@ def main(argv=None):
     ap.add_argument("--cpu-sample", type=int, default=512)
     ap.add_argument("--ref-sample", type=int, default=64)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--store-logits", action="store_true",
+                    help="ablation: keep each chunk's logits instead of recomputing them")
     ap.add_argument("--allow-short-warmup", action="store_true",
                     help="profiling runs only: honour --warmup below 3")
     args = ap.parse_args(argv)

@@ -23,6 +23,8 @@ LIB_PATH = os.path.join(HERE, "libkdtopk.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "kd_topk_kl.h")
 
 KD_OK = 0
+KD_FLAG_ACCUMULATE = 1
+KD_FLAG_STORE_LOGITS = 2
 STATUS_NAMES = {
     0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_ALIGNMENT", 3: "KD_ERR_INDEX",
     4: "KD_ERR_OOM", 5: "KD_ERR_CUDA", 6: "KD_ERR_TIMEOUT", 7: "KD_ERR_NOT_IMPLEMENTED",
@@ -69,6 +71,11 @@ def lib() -> ctypes.CDLL:
     L.kd_topk_kl_fwd_bwd_masked.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
                                              i32, vp, vp, vp, vp, sz, vp]
     L.kd_topk_kl_fwd_bwd_masked.restype = i32
+    L.kd_topk_kl_fwd_bwd_flags.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
+                                            ctypes.c_uint, vp, vp, vp, vp, sz, vp]
+    L.kd_topk_kl_fwd_bwd_flags.restype = i32
+    L.kd_topk_kl_workspace_size_flags.argtypes = [i64, i32, i32, i32, i32, ctypes.c_uint]
+    L.kd_topk_kl_workspace_size_flags.restype = sz
     L.kd_topk_kl_debug.argtypes = common + [vp, sz, vp, ctypes.POINTER(_DebugOpts)]
     L.kd_topk_kl_debug.restype = i32
     L.kd_topk_kl_workspace_size.argtypes = [i64, i32, i32, i32, i32]
@@ -181,18 +188,25 @@ def kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
     return float(loss.value)
 
 
+def _check_mask(token_mask, N):
+    import torch
+    if token_mask is None:
+        return None
+    if token_mask.dtype == torch.bool:
+        token_mask = token_mask.view(torch.uint8)
+    if token_mask.dtype != torch.uint8 or token_mask.shape != (N,) or not token_mask.is_cuda \
+            or not token_mask.is_contiguous():
+        raise ValueError("token_mask must be a contiguous uint8/bool CUDA tensor of shape [N]")
+    return token_mask
+
+
 def kd_topk_kl_fwd_bwd_masked(hidden, W, topk_idx, topk_logit, token_mask, T: float,
                               chunk: int, grad_hidden, grad_W, workspace, accumulate=False,
                               stream=None) -> float:
     """Per-token mask (uint8/bool [N] CUDA tensor or None) and accumulate flag."""
     import torch
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
-    if token_mask is not None:
-        if token_mask.dtype == torch.bool:
-            token_mask = token_mask.view(torch.uint8)
-        if token_mask.dtype != torch.uint8 or token_mask.shape != (N,) or not token_mask.is_cuda \
-                or not token_mask.is_contiguous():
-            raise ValueError("token_mask must be a contiguous uint8/bool CUDA tensor of shape [N]")
+    token_mask = _check_mask(token_mask, N)
     loss = ctypes.c_float(0.0)
     st = lib().kd_topk_kl_fwd_bwd_masked(
         _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
@@ -200,6 +214,26 @@ def kd_topk_kl_fwd_bwd_masked(hidden, W, topk_idx, topk_logit, token_mask, T: fl
         _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream_handle(stream))
     _check(st, "kd_topk_kl_fwd_bwd_masked")
+    return float(loss.value)
+
+
+def kd_topk_kl_workspace_size_flags(N: int, H: int, V: int, K: int, chunk: int,
+                                    flags: int) -> int:
+    return int(lib().kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, int(flags)))
+
+
+def kd_topk_kl_fwd_bwd_flags(hidden, W, topk_idx, topk_logit, token_mask, T: float, chunk: int,
+                             flags: int, grad_hidden, grad_W, workspace, stream=None) -> float:
+    """Mask (or None) and KD_FLAG_* flags (accumulate, store logits)."""
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    token_mask = _check_mask(token_mask, N)
+    loss = ctypes.c_float(0.0)
+    st = lib().kd_topk_kl_fwd_bwd_flags(
+        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
+        float(T), int(chunk), int(flags), ctypes.addressof(loss), _ptr(grad_hidden),
+        _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd_flags")
     return float(loss.value)
 
 

@@ -35,10 +35,11 @@ constexpr int kMaxK = 8192;
 // bracketed by two CUDA events on the launch stream; after the call's final
 // synchronisation the elapsed times are added to per-kind totals.
 enum ProfKind { PK_PREP = 0, PK_FWD, PK_LSE, PK_DZ, PK_GRAD_H, PK_SPLIT_RED, PK_GRAD_W,
-                PK_FINAL, PK_TRANSPOSE, PK_COUNT };
+                PK_FINAL, PK_TRANSPOSE, PK_MASK, PK_DZ_EW, PK_COUNT };
 const char* const kProfNames[PK_COUNT] = {"prep_topk", "gemm_fwd_lse_gather", "lse_loss_fold",
                                           "gemm_bwd_dz", "gemm_grad_hidden", "split_reduce",
-                                          "gemm_grad_W", "loss_final", "transpose_chunk"};
+                                          "gemm_grad_W", "loss_final", "transpose_chunk",
+                                          "mask_count", "dz_from_logits"};
 
 struct Profiler {
   std::mutex mu;
@@ -152,8 +153,9 @@ struct Plan {
   int hp;         // mth * its tile M: rows of one split's grad_hidden^T partial
   int splits;     // K splits of the grad_hidden^T GEMM
   int sms;
+  bool store_z;   // keep each chunk's fp32 logits instead of recomputing them
   size_t off_status, off_sid, off_sp, off_perm, off_ent, off_psum, off_loss_rows, off_lse2,
-      off_zg, off_part, off_dz, off_k4, off_hT, total;
+      off_zg, off_part, off_dz, off_k4, off_hT, off_z, total;
 };
 
 bool sizes_ok(long long N, int H, int V, int K, int chunk) {
@@ -183,9 +185,9 @@ int pick_splits(int units, int kb_total, int sms) {
   return best;
 }
 
-Plan make_plan(long long N, int H, int V, int K, int chunk, int sms) {
+Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_z = false) {
   Plan p{};
-  p.N = N; p.H = H; p.V = V; p.K = K; p.sms = sms;
+  p.N = N; p.H = H; p.V = V; p.K = K; p.sms = sms; p.store_z = store_z;
   long long c = cdiv(chunk, 128) * 128;
   const long long cmax = cdiv(N, 128) * 128;
   if (c > cmax) c = cmax;
@@ -212,6 +214,7 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms) {
   p.off_dz = take(2ull * c * V);
   p.off_k4 = take(4ull * p.splits * p.hp * c);
   p.off_hT = take(2ull * H * c);
+  p.off_z = store_z ? take(4ull * c * V) : 0;
   p.total = o;
   return p;
 }
@@ -244,15 +247,20 @@ kd_status validate(const void* hidden, const void* W, const int32_t* idx, const 
 
 // The whole path on stream s.  mask (optional, device [N]): nonzero = the
 // token counts; the mean runs over the valid tokens and masked tokens get
-// zero gradient rows.  accumulate: add into grad_hidden / grad_W.
+// zero gradient rows.  flags: KD_FLAG_ACCUMULATE adds into grad_hidden /
+// grad_W; KD_FLAG_STORE_LOGITS keeps each chunk's fp32 logits from the
+// forward GEMM and forms dZ from them instead of recomputing the GEMM.
 kd_status run(const void* hidden, const void* W, const int32_t* idx, const float* logit,
               long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
               float* gW, void* ws, size_t ws_bytes, cudaStream_t s, const kd_debug_opts* opts,
-              const uint8_t* mask = nullptr, int accumulate = 0) {
+              const uint8_t* mask = nullptr, unsigned flags = 0) {
+  const int accumulate = (flags & KD_FLAG_ACCUMULATE) ? 1 : 0;
+  const bool store_z = (flags & KD_FLAG_STORE_LOGITS) != 0;
+  if (flags & ~(KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS)) return KD_ERR_INVALID_ARG;
   kd_status st = validate(hidden, W, idx, logit, N, H, V, K, T, chunk, loss, gh, gW);
   if (st != KD_OK) return st;
   if (mask && !is_device_ptr(mask)) return KD_ERR_INVALID_ARG;
-  const Plan p = make_plan(N, H, V, K, chunk, device_sms());
+  const Plan p = make_plan(N, H, V, K, chunk, device_sms(), store_z);
   if (!ws || ws_bytes < p.total) return KD_ERR_OOM;
   prof().used = 0;
   if (!aligned(ws, 256)) return KD_ERR_ALIGNMENT;
@@ -272,6 +280,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   void* dz = base + p.off_dz;
   float* k4 = reinterpret_cast<float*>(base + p.off_k4);
   void* hT = base + p.off_hT;
+  float* zbuf = store_z ? reinterpret_cast<float*>(base + p.off_z) : nullptr;
 
   const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
   float* dbg_lse = opts ? opts->lse : nullptr;
@@ -293,6 +302,8 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   ok &= make_map(&tm_dz_mn, BF16, 2, dz, V, p.chunk, 64, 64);
   ok &= make_map(&tm_ht_k, BF16, 2, hT, p.chunk, H, 64, b_box_rows(kd::GV_GRAD_W));
   ok &= make_map(&tm_gw, F32, 4, gW, H, V, 32, 32);
+  CUtensorMap tm_z_st;
+  if (store_z) ok &= make_map(&tm_z_st, F32, 4, zbuf, V, p.chunk, 32, 32);
   if (!ok) {
     std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed");
     return KD_ERR_CUDA;
@@ -305,6 +316,7 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   // masked calls: n_valid and the gradient scale 1/(T n_valid) on the device
   const float* alpha_dev = nullptr;
   if (mask) {
+    ProfScope ps_(PK_MASK, s);
     KD_CUDA(kd::launch_mask_count(mask, N, T, dst, s));
     alpha_dev = &dst->alpha;
   }
@@ -326,13 +338,27 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
     e.sid = sid; e.sp = sp; e.perm = perm; e.part = part; e.zg = zg; e.lse2 = lse2;
     e.dbg_found = dbg_found;
     e.mask = mask;
-    { ProfScope ps_(PK_FWD, s); KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e, s)); }
+    if (store_z) {
+      ProfScope ps_(PK_FWD, s);
+      KD_CUDA(kd::launch_gemm(kd::GV_FWDZ, tm_hid_k, tm_w_k, tm_z_st, g, e, s));
+    } else {
+      ProfScope ps_(PK_FWD, s);
+      KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e, s));
+    }
 
     { ProfScope ps_(PK_LSE, s); KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, mask, lse2,
                                 loss_rows, dbg_lse, dbg_zg, s)); }
 
     g.inject_timeout = 0;
-    { ProfScope ps_(PK_DZ, s); KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e, s)); }
+    if (store_z) {
+      // rows up to the GEMMs' reach get a dZ row (zeros past the chunk)
+      const int cover = static_cast<int>(std::min<long long>(p.chunk, cdiv(cj, 256) * 256));
+      ProfScope ps_(PK_DZ_EW, s);
+      KD_CUDA(kd::launch_dz_from_z(zbuf, V, cj, cover, lse2, scale2, mask, row0, sid, sp, K, dz, s));
+    } else {
+      ProfScope ps_(PK_DZ, s);
+      KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e, s));
+    }
 
     // grad_hidden rows of this chunk: (dZ W)^T = W^T dZ^T, split-K over the
     // vocabulary, then an ordered transposing reduction of the splits
@@ -406,7 +432,24 @@ kd_status kd_topk_kl_fwd_bwd_masked(const void* hidden, const void* W, const int
                                     void* stream) {
   return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
              workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, token_mask,
-             accumulate);
+             accumulate ? KD_FLAG_ACCUMULATE : 0u);
+}
+
+size_t kd_topk_kl_workspace_size_flags(int64_t N, int H, int V, int K, int chunk,
+                                       unsigned flags) {
+  if (!sizes_ok(N, H, V, K, chunk)) return 0;
+  if (flags & ~(KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS)) return 0;
+  return make_plan(N, H, V, K, chunk, device_sms(), (flags & KD_FLAG_STORE_LOGITS) != 0).total;
+}
+
+kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int32_t* topk_idx,
+                                   const float* topk_logit, const uint8_t* token_mask,
+                                   int64_t N, int H, int V, int K, float T, int chunk,
+                                   unsigned flags, float* loss, float* grad_hidden, float* grad_W,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
+             workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, token_mask,
+             flags);
 }
 
 kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* topk_idx,

@@ -7,7 +7,7 @@ namespace kd {
 
 struct DevStatus;
 
-enum EpiKind { EPI_FWD = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_ACC = 3 };
+enum EpiKind { EPI_FWD = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_ACC = 3, EPI_FWDZ = 4 };
 enum Order { ORDER_M_FAST = 0, ORDER_N_FAST = 1, ORDER_SPLIT = 2 };
 enum WaitSite { SITE_PROD = 1, SITE_MMA_FULL = 2, SITE_MMA_TEMPTY = 3, SITE_EPI = 4,
                 SITE_INJECT = 5, SITE_DRAIN = 6 };
@@ -38,7 +38,7 @@ struct EpiArgs {
   const int* sid;        // [N][K] ids sorted ascending per row
   const float* sp;       // [N][K] teacher p in the same order
   const int* perm;       // [N][K] sorted position -> original k
-  float2* part;          // EPI_FWD: [n_tiles][c_alloc] (max, sum) in log2 units
+  float2* part;          // EPI_FWD(Z): [n_tiles][c_alloc] (max, sum) in log2 units
   float* zg;             // EPI_FWD: [c_alloc][K] z at the sorted ids
   const float* lse2;     // EPI_DZ: [c_alloc] log2-sum-exp2 of z*log2e/T
   int* dbg_found;        // EPI_FWD: optional [N][K] column at which id k was found

@@ -26,6 +26,8 @@
 //              teacher ids that fall in the tile (forward of the loss).
 //   EPI_DZ   : G = 2^(z*log2e/T - lse2) - sum of teacher p at the row's ids
 //              in the tile, stored as bf16 through TMA (backward recompute).
+//   EPI_FWDZ : EPI_FWD, and z itself stored as fp32 through TMA (the
+//              logits kept for a backward pass without recompute).
 //   EPI_F32  : alpha * D stored as fp32 through TMA.
 //   EPI_ACC  : alpha * D added into an fp32 tensor by TMA reduce-add
 //              (plain store when `first`).
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int* ids = nullptr;
       float lse2 = 0.f;
       const int v0 = t.n * C::BN;
-      if constexpr (C::KIND == EPI_FWD || C::KIND == EPI_DZ) {
+      if constexpr (C::KIND == EPI_FWD || C::KIND == EPI_FWDZ || C::KIND == EPI_DZ) {
         if (row_ok) {
           ids = e.sid + static_cast<long long>(e.grow0 + mrow) * e.K;
           hit = lower_bound_ids(ids, e.K, v0);
@@ -385,7 +387,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       const uint32_t tb = tmem_base + lane_off + acc * C::BN;
 
-      if constexpr (C::KIND == EPI_FWD) {
+      if constexpr (C::KIND == EPI_FWD || C::KIND == EPI_FWDZ) {
         float m_run = -INFINITY, s_run = 0.f;
 #pragma unroll 1
         for (int b = 0; b < C::BN / 32; ++b) {
@@ -407,6 +409,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const int nvalid = e.cols_valid - (v0 + c0);   // warp-uniform
           if (nvalid <= 0) continue;
+          if constexpr (C::KIND == EPI_FWDZ) {
+            if (box_row0 < e.c_alloc) {                  // warp-uniform: inside the z tensor
+              const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+              stage_row_128B(box, lane, r);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, box_row0);
+                bulk_commit();
+              }
+              ++sub_ctr;
+            }
+          }
           float bm = -INFINITY;
 #pragma unroll
           for (int j = 0; j < 32; ++j)

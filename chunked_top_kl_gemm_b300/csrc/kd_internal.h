@@ -29,6 +29,7 @@ enum GemmVariant {
   GV_TEST_KM2 = 13,
   GV_TEST_MK2 = 14,
   GV_TEST_MM2 = 15,
+  GV_FWDZ = 16,        // K1 that also stores the chunk's fp32 logits
 };
 
 // Tile width of the N dimension of each variant.
@@ -59,6 +60,13 @@ cudaError_t launch_split_reduce_t(const float* part, int splits, long long split
                                   int c_alloc, int rows_valid, int H, float alpha,
                                   const float* alpha_dev, int accumulate, float* out,
                                   cudaStream_t s);
+
+// dZ of rows [0, rows_cover) of a chunk from its stored fp32 logits z
+// [rows][V] (rows >= rows_valid and masked rows get zeros), then the
+// cached-id columns.
+cudaError_t launch_dz_from_z(const float* z, int V, int rows_valid, int rows_cover,
+                             const float* lse2, float scale2, const uint8_t* mask, int grow0,
+                             const int* sid, const float* sp, int K, void* dz, cudaStream_t s);
 
 cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStatus* st,
                               cudaStream_t s);

@@ -39,6 +39,8 @@ using CfgFwd = GemmCfg<256, false, false, 7, EPI_FWD, true>;
 using CfgDz = GemmCfg<256, false, false, 6, EPI_DZ, true>;
 using CfgGradH = GemmCfg<256, true, false, 6, EPI_F32, true>;   // grad_hidden^T = W^T dZ^T
 using CfgGradW = GemmCfg<256, true, false, 6, EPI_ACC, true>;   // grad_W = dZ^T h_c
+// forward that also keeps the chunk's fp32 logits (backward without recompute)
+using CfgFwdZ = GemmCfg<256, false, false, 6, EPI_FWDZ, true>;
 // single-CTA forms (128 x BN tiles), kept for the GEMM-core tests
 using CfgTestKK = GemmCfg<256, false, false, 4, EPI_F32>;
 using CfgTestKM = GemmCfg<192, false, true, 4, EPI_F32>;
@@ -134,7 +136,7 @@ static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const 
   X(GV_TEST_MM, CfgTestMM) X(GV_TEST_KK192, CfgTestKK192) X(GV_TEST_KM256, CfgTestKM256) \
   X(GV_TEST_MK256, CfgTestMK256) X(GV_TEST_MM256, CfgTestMM256)                         \
   X(GV_TEST_KK2, CfgTestKK2) X(GV_TEST_KM2, CfgTestKM2) X(GV_TEST_MK2, CfgTestMK2)       \
-  X(GV_TEST_MM2, CfgTestMM2)
+  X(GV_TEST_MM2, CfgTestMM2) X(GV_FWDZ, CfgFwdZ)
 
 int gemm_bn(int variant) {
 #define X(V, C) case V: return C::BN;
@@ -439,6 +441,71 @@ cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc,
   dim3 grid((c_alloc + 63) / 64, (H + 63) / 64);
   kd_transpose_chunk<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hid), rows_valid,
                                           c_alloc, H, static_cast<__nv_bfloat16*>(hT));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dZ from stored logits
+// The backward's dZ without recomputing the logits: for rows < rows_cover,
+//   dZ[r][v] = bf16(2^(z[r][v] * scale2 - lse2[r]))      (0 for r >= rows_valid
+// and for masked rows), eight columns per thread; kd_dz_fixup then rewrites
+// the cached-id columns.  Both round exactly as the recompute GEMM's epilogue
+// does, so the two backward forms give bitwise the same dZ.
+__global__ void __launch_bounds__(256) kd_dz_from_z(const float* __restrict__ z, int V,
+                                                    int rows_valid, const float* __restrict__ lse2,
+                                                    float scale2, const uint8_t* __restrict__ mask,
+                                                    int grow0, __nv_bfloat16* __restrict__ dz) {
+  const int r = blockIdx.y;
+  const int v = (blockIdx.x * 256 + threadIdx.x) * 8;
+  if (v >= V) return;                       // V is a multiple of 8
+  const long long off = static_cast<long long>(r) * V + v;
+  uint4 out = make_uint4(0u, 0u, 0u, 0u);
+  const bool live = r < rows_valid && (!mask || mask[grow0 + r] != 0);
+  if (live) {
+    const float l2 = lse2[r];
+    const float4 a = *reinterpret_cast<const float4*>(z + off);
+    const float4 b = *reinterpret_cast<const float4*>(z + off + 4);
+    out.x = pack_bf16x2(ex2_approx(fmaf(a.x, scale2, -l2)), ex2_approx(fmaf(a.y, scale2, -l2)));
+    out.y = pack_bf16x2(ex2_approx(fmaf(a.z, scale2, -l2)), ex2_approx(fmaf(a.w, scale2, -l2)));
+    out.z = pack_bf16x2(ex2_approx(fmaf(b.x, scale2, -l2)), ex2_approx(fmaf(b.y, scale2, -l2)));
+    out.w = pack_bf16x2(ex2_approx(fmaf(b.z, scale2, -l2)), ex2_approx(fmaf(b.w, scale2, -l2)));
+  }
+  *reinterpret_cast<uint4*>(dz + off) = out;
+}
+
+// dZ at the cached ids: g - p for each distinct id of a live row, with the
+// teacher masses of a repeated id subtracted one by one in sorted order.
+__global__ void __launch_bounds__(256) kd_dz_fixup(const float* __restrict__ z, int V,
+                                                   int rows_valid, int K,
+                                                   const float* __restrict__ lse2, float scale2,
+                                                   const uint8_t* __restrict__ mask, int grow0,
+                                                   const int* __restrict__ sid,
+                                                   const float* __restrict__ sp,
+                                                   __nv_bfloat16* __restrict__ dz) {
+  const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= static_cast<long long>(rows_valid) * K) return;
+  const int r = static_cast<int>(i / K), k = static_cast<int>(i % K);
+  const long long g = static_cast<long long>(grow0) + r;
+  if (mask && mask[g] == 0) return;
+  const int* ids = sid + g * K;
+  const float* ps = sp + g * K;
+  const int id = ids[k];
+  if (k > 0 && ids[k - 1] == id) return;     // the run's first entry writes
+  float val = ex2_approx(fmaf(z[static_cast<long long>(r) * V + id], scale2, -lse2[r]));
+  for (int j = k; j < K && ids[j] == id; ++j) val -= ps[j];
+  dz[static_cast<long long>(r) * V + id] = __float2bfloat16_rn(val);
+}
+
+cudaError_t launch_dz_from_z(const float* z, int V, int rows_valid, int rows_cover,
+                             const float* lse2, float scale2, const uint8_t* mask, int grow0,
+                             const int* sid, const float* sp, int K, void* dz, cudaStream_t s) {
+  dim3 grid((V / 8 + 255) / 256, rows_cover);
+  kd_dz_from_z<<<grid, 256, 0, s>>>(z, V, rows_valid, lse2, scale2, mask, grow0,
+                                    static_cast<__nv_bfloat16*>(dz));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long n = static_cast<long long>(rows_valid) * K;
+  kd_dz_fixup<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+      z, V, rows_valid, K, lse2, scale2, mask, grow0, sid, sp, static_cast<__nv_bfloat16*>(dz));
   return cudaGetLastError();
 }
 

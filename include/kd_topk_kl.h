@@ -138,6 +138,37 @@ kd_status kd_topk_kl_fwd_bwd_masked(const void* hidden, const void* W, const int
                                     float* grad_W, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/* Flags of kd_topk_kl_fwd_bwd_flags / kd_topk_kl_workspace_size_flags. */
+#define KD_FLAG_ACCUMULATE 1u     /* add into grad_hidden / grad_W instead of overwriting */
+#define KD_FLAG_STORE_LOGITS 2u   /* keep each chunk's logits between forward and backward */
+
+/*
+ * Workspace bytes for kd_topk_kl_fwd_bwd_flags with these flags (0 when the
+ * sizes or the flags are invalid).  KD_FLAG_STORE_LOGITS adds chunk x V x 4
+ * bytes (the chunk's fp32 logits).
+ */
+size_t kd_topk_kl_workspace_size_flags(int64_t N, int H, int V, int K, int chunk,
+                                       unsigned flags);
+
+/*
+ * kd_topk_kl_fwd_bwd_masked with flags.
+ *
+ * KD_FLAG_STORE_LOGITS is an ablation of the recompute the pages describe
+ * (glonce.com, body: the fused loss recomputes chunks during the backward
+ * pass instead of storing them, and at 8K context that extra projection
+ * costs some speed).  The forward GEMM also writes the chunk's fp32 logits
+ * to the workspace, and the backward forms dZ from them with an elementwise
+ * kernel instead of recomputing the GEMM: 6 N H V instead of 8 N H V flops,
+ * for chunk x V x 4 more bytes of workspace.  The logits are the very values
+ * the recompute would produce, and dZ is rounded the same way, so the
+ * results are bitwise those of the recompute path.
+ */
+kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int32_t* topk_idx,
+                                   const float* topk_logit, const uint8_t* token_mask,
+                                   int64_t N, int H, int V, int K, float T, int chunk,
+                                   unsigned flags, float* loss, float* grad_hidden, float* grad_W,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Test and diagnosis options for kd_topk_kl_debug.  Each output pointer may
  * be NULL (not written).

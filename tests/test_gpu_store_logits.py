@@ -1,0 +1,100 @@
+"""The store-logits backward (KD_FLAG_STORE_LOGITS) against the recompute path (GPU).
+
+With the flag, the forward GEMM also writes each chunk's fp32 logits and
+the backward forms dZ from them elementwise instead of recomputing the
+GEMM.  The stored logits are the values the recompute produces and dZ is
+rounded the same way, so loss and gradients must equal the recompute
+path's bit for bit -- with and without a token mask, and when accumulating.
+"""
+import numpy as np
+import pytest
+import torch
+
+import chunked_top_kl_gemm_b300 as kd
+import oracle
+import workloads
+from tests.gpu_util import GRAD_REL_L2, LOSS_RTOL, ensure_lib, rel_l2, to_device
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "ragged": workloads.custom("z_ragged", N=300, H=200, V=1000, K=7, T=0.7, chunk=128),
+    "mid": workloads.custom("z_mid", N=640, H=576, V=8192, K=100, T=1.0, chunk=256,
+                            hidden_rms_norm=True, teacher="zipf"),
+    "spiky_T2": workloads.custom("z_spiky", N=256, H=128, V=2048, K=32, T=2.0, chunk=128,
+                                 hidden_rms_norm=True, teacher="zipf", spike_frac=0.1),
+    "kv": workloads.custom("z_kv", N=130, H=72, V=136, K=136, T=1.5, chunk=128),
+}
+
+
+def _run(inp, T, chunk, flags, mask=None, gh=None, gW=None):
+    h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
+    N, H = h.shape
+    V, K = W.shape[0], idx.shape[1]
+    gh = torch.full((N, H), float("nan"), device="cuda") if gh is None else gh
+    gW = torch.full((V, H), float("nan"), device="cuda") if gW is None else gW
+    nbytes = kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, flags)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    loss = kd.kd_topk_kl_fwd_bwd_flags(h, W, idx, lg, mask, T, chunk, flags, gh, gW, ws)
+    torch.cuda.synchronize()
+    return loss, gh, gW
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("masked", [False, True])
+def test_store_logits_equals_recompute_bitwise(name, masked):
+    ensure_lib()
+    cfg = CASES[name]
+    inp = to_device(workloads.make_inputs(cfg, seed=31))
+    mask = None
+    if masked:
+        g = torch.Generator().manual_seed(7)
+        mask = (torch.rand(cfg.N, generator=g) < 0.6).to(torch.uint8).cuda()
+    a = _run(inp, cfg.T, cfg.chunk, 0, mask)
+    b = _run(inp, cfg.T, cfg.chunk, kd.KD_FLAG_STORE_LOGITS, mask)
+    assert a[0] == b[0]
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_store_logits_with_accumulate_and_repeated_ids():
+    ensure_lib()
+    cfg = workloads.custom("z_dup", N=200, H=64, V=512, K=6, T=1.0, chunk=128)
+    inp = workloads.make_inputs(cfg, seed=5)
+    idx = inp["topk_idx"].clone()
+    idx[::3, 1] = idx[::3, 0]            # repeated ids: the masses subtract one by one
+    inp["topk_idx"] = idx
+    inp = to_device(inp)
+    g = torch.Generator(device="cuda").manual_seed(2)
+    gh0 = torch.randn((cfg.N, cfg.H), generator=g, device="cuda") * 1e-3
+    gW0 = torch.randn((cfg.V, cfg.H), generator=g, device="cuda") * 1e-3
+    acc = kd.KD_FLAG_ACCUMULATE
+    a = _run(inp, cfg.T, cfg.chunk, acc, gh=gh0.clone(), gW=gW0.clone())
+    b = _run(inp, cfg.T, cfg.chunk, acc | kd.KD_FLAG_STORE_LOGITS, gh=gh0.clone(),
+             gW=gW0.clone())
+    assert a[0] == b[0] and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    want = oracle.fused_topk_kl(inp["hidden"].cpu(), inp["W"].cpu(), idx, inp["topk_logit"].cpu(),
+                                cfg.T)
+    assert abs(b[0] - want["loss"]) <= LOSS_RTOL * abs(want["loss"])
+    assert rel_l2((b[2] - gW0).cpu().numpy(), want["grad_W"]) <= GRAD_REL_L2
+
+
+def test_store_logits_full_vocabulary_two_chunks():
+    """Two 2048-row chunks of the GPT-OSS-like head (V = 201,088): the same
+    launch shapes as the benchmark's store-logits mode."""
+    ensure_lib()
+    cfg = workloads.CONFIGS["gptoss32k"]
+    inp = workloads.make_inputs(cfg, seed=3, device="cuda", n_rows=4096)
+    a = _run(inp, cfg.T, cfg.chunk, 0)
+    b = _run(inp, cfg.T, cfg.chunk, kd.KD_FLAG_STORE_LOGITS)
+    assert a[0] == b[0]
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_workspace_grows_by_the_chunk_logits():
+    ensure_lib()
+    N, H, V, K, chunk = 32768, 2880, 201088, 100, 2048
+    base = kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, 0)
+    assert base == kd.kd_topk_kl_workspace_size(N, H, V, K, chunk)
+    stored = kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, kd.KD_FLAG_STORE_LOGITS)
+    assert 4 * chunk * V <= stored - base < 4 * chunk * V + 512
+    assert kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, 8) == 0
