@@ -372,6 +372,72 @@ def run_gpu(args):
     return 0
 
 
+# ------------------------------------------------------------------ sweep
+# The shape of the pages' isolated output-projection benchmark (glonce.com,
+# body; ainewsbank.com, "What the long-context measurements show"): peak
+# memory should stay flat in N x V and grow only with the per-token tensors,
+# and the chunk size trades workspace for speed.  One JSON line per point.
+SWEEP_POINTS = (
+    [("tiny", None, None), ("llama3b", None, None)]
+    + [("gptoss32k", n, 2048) for n in (8192, 32768, 65536, 131072, 262144)]
+    + [("long64k", None, None)]
+    + [("ext256k", None, c) for c in (1024, 2048, 4096, 8192)]
+)
+
+
+def run_sweep(args):
+    import dataclasses
+
+    import torch
+
+    import chunked_top_kl_gemm_b300 as kd
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kd.lib()
+    peaks, _ = load_peaks()
+    for name, n_tokens, chunk in SWEEP_POINTS:
+        cfg = workloads.CONFIGS[name]
+        if n_tokens:
+            cfg = dataclasses.replace(cfg, N=n_tokens, name=f"{name}_n{n_tokens}")
+        chunk = chunk or cfg.chunk
+        N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        mem0 = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        inp = workloads.make_inputs(cfg, seed=0, device=dev)
+        gh = torch.empty((N, H), dtype=torch.float32, device=dev)
+        gW = torch.empty((V, H), dtype=torch.float32, device=dev)
+        ws = kd.alloc_workspace(N, H, V, K, chunk, device=dev)
+        args_ = (inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"], T, chunk, gh, gW, ws)
+        loss = kd.kd_topk_kl_fwd_bwd_ex(*args_)
+        torch.cuda.synchronize(dev)
+        peak = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
+        steps = max(1, min(args.steps, int(4e13 // cfg.flops) + 1))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            loss = kd.kd_topk_kl_fwd_bwd_ex(*args_)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        tflops = cfg.flops / t / 1e12
+        print(json.dumps({
+            "sweep": "memory_and_throughput", "workload": cfg.name, "N": N, "H": H, "V": V,
+            "K": K, "T": T, "chunk": chunk, "steps": steps, "tokens_per_s": N / t,
+            "ms_per_step": t * 1e3, "tflops": tflops,
+            "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
+            "peak_gib": peak,
+            "inputs_gib": sum(workloads.bytes_of_inputs(cfg).values()) / 2**30,
+            "grads_gib": 4 * (N * H + V * H) / 2**30,
+            "workspace_gib": ws.numel() / 2**30,
+            "dense_fp32_logits_gib": 4 * N * V / 2**30, "loss": loss}), flush=True)
+        del inp, gh, gW, ws, args_
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -389,7 +455,12 @@ def main(argv=None):
                     help="ablation: keep each chunk's logits instead of recomputing them")
     ap.add_argument("--allow-short-warmup", action="store_true",
                     help="profiling runs only: honour --warmup below 3")
+    ap.add_argument("--sweep", action="store_true",
+                    help="peak memory and throughput over token counts and chunk sizes "
+                         "(one JSON line per point)")
     args = ap.parse_args(argv)
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
