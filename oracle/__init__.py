@@ -15,3 +15,4 @@ from .kl_topk import (  # noqa: F401
     grad_W_rows,
     to_f64,
 )
+from .topk_cache import topk_cache, topk_rows  # noqa: F401
