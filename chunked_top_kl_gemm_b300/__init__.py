@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
     L.kd_topk_kl_fwd_bwd_flags.restype = i32
     L.kd_topk_kl_workspace_size_flags.argtypes = [i64, i32, i32, i32, i32, ctypes.c_uint]
     L.kd_topk_kl_workspace_size_flags.restype = sz
+    L.kd_topk_cache_workspace_size.argtypes = [i64, i32, i32, i32, i32]
+    L.kd_topk_cache_workspace_size.restype = sz
+    L.kd_topk_cache_build.argtypes = [vp, vp, i64, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.kd_topk_cache_build.restype = i32
     L.kd_topk_kl_debug.argtypes = common + [vp, sz, vp, ctypes.POINTER(_DebugOpts)]
     L.kd_topk_kl_debug.restype = i32
     L.kd_topk_kl_workspace_size.argtypes = [i64, i32, i32, i32, i32]
@@ -235,6 +239,39 @@ def kd_topk_kl_fwd_bwd_flags(hidden, W, topk_idx, topk_logit, token_mask, T: flo
         _stream_handle(stream))
     _check(st, "kd_topk_kl_fwd_bwd_flags")
     return float(loss.value)
+
+
+def kd_topk_cache_workspace_size(N: int, H: int, V: int, K: int, chunk: int) -> int:
+    return int(lib().kd_topk_cache_workspace_size(N, H, V, K, chunk))
+
+
+def kd_topk_cache_build(hidden, W, K: int, chunk: int = 2048, *, topk_idx=None,
+                        topk_logit=None, workspace=None, stream=None):
+    """The offline teacher cache: (int32 ids [N,K], fp32 logits [N,K]) of the
+    K largest logits of ``hidden @ W.T`` per token, decreasing, ties by id."""
+    import torch
+    if hidden.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("hidden and W must be bfloat16")
+    if not (hidden.is_cuda and W.is_cuda and hidden.is_contiguous() and W.is_contiguous()):
+        raise ValueError("hidden and W must be contiguous CUDA tensors")
+    N, H = hidden.shape
+    V = W.shape[0]
+    dev = hidden.device
+    if topk_idx is None:
+        topk_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    if topk_logit is None:
+        topk_logit = torch.empty((N, K), dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = kd_topk_cache_workspace_size(N, H, V, K, chunk)
+        if nbytes == 0:
+            raise KdError(1, "kd_topk_cache_workspace_size")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = lib().kd_topk_cache_build(_ptr(hidden), _ptr(W), N, H, V, int(K), int(chunk),
+                                   _ptr(topk_idx), _ptr(topk_logit), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   _stream_handle(stream))
+    _check(st, "kd_topk_cache_build")
+    return topk_idx, topk_logit
 
 
 def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad_hidden,

@@ -35,11 +35,13 @@ constexpr int kMaxK = 8192;
 // bracketed by two CUDA events on the launch stream; after the call's final
 // synchronisation the elapsed times are added to per-kind totals.
 enum ProfKind { PK_PREP = 0, PK_FWD, PK_LSE, PK_DZ, PK_GRAD_H, PK_SPLIT_RED, PK_GRAD_W,
-                PK_FINAL, PK_TRANSPOSE, PK_MASK, PK_DZ_EW, PK_COUNT };
+                PK_FINAL, PK_TRANSPOSE, PK_MASK, PK_DZ_EW, PK_CACHE_GEMM, PK_CACHE_SELECT,
+                PK_COUNT };
 const char* const kProfNames[PK_COUNT] = {"prep_topk", "gemm_fwd_lse_gather", "lse_loss_fold",
                                           "gemm_bwd_dz", "gemm_grad_hidden", "split_reduce",
                                           "gemm_grad_W", "loss_final", "transpose_chunk",
-                                          "mask_count", "dz_from_logits"};
+                                          "mask_count", "dz_from_logits", "cache_gemm_logits",
+                                          "cache_topk_select"};
 
 struct Profiler {
   std::mutex mu;
@@ -532,6 +534,106 @@ kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N
   KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
   KD_CUDA(cudaFreeAsync(dst, s));
   KD_CUDA(cudaStreamSynchronize(s));
+  if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
+  return KD_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- top-K cache builder
+namespace {
+
+struct CachePlan {
+  int chunk, n_chunks, vt;
+  size_t off_status, off_part, off_z, total;
+};
+
+CachePlan make_cache_plan(long long N, int V, int chunk) {
+  CachePlan p{};
+  long long c = cdiv(chunk, 128) * 128;
+  const long long cmax = cdiv(N, 128) * 128;
+  if (c > cmax) c = cmax;
+  p.chunk = static_cast<int>(c);
+  p.n_chunks = static_cast<int>(cdiv(N, c));
+  p.vt = static_cast<int>(cdiv(V, kd::gemm_bn(kd::GV_FWDZ)));
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, 256); return at; };
+  p.off_status = take(sizeof(DevStatus));
+  p.off_part = take(sizeof(float2) * p.vt * c);
+  p.off_z = take(4ull * c * V);
+  p.total = o;
+  return p;
+}
+
+bool cache_sizes_ok(long long N, int H, int V, int K, int chunk) {
+  return N >= 1 && N <= 0x7fffffffLL && H >= 8 && H % 8 == 0 && V >= 8 && V % 8 == 0 &&
+         K >= 1 && K <= V && K <= 8192 && chunk >= 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kd_topk_cache_workspace_size(int64_t N, int H, int V, int K, int chunk) {
+  if (!cache_sizes_ok(N, H, V, K, chunk)) return 0;
+  return make_cache_plan(N, V, chunk).total;
+}
+
+kd_status kd_topk_cache_build(const void* hidden, const void* W, int64_t N, int H, int V, int K,
+                              int chunk, int32_t* topk_idx, float* topk_logit, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!hidden || !W || !topk_idx || !topk_logit || !workspace) return KD_ERR_INVALID_ARG;
+  if (!cache_sizes_ok(N, H, V, K, chunk)) return KD_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(topk_idx, 4) ||
+      !aligned(topk_logit, 4) || !aligned(workspace, 256))
+    return KD_ERR_ALIGNMENT;
+  if (!is_device_ptr(hidden) || !is_device_ptr(W) || !is_device_ptr(topk_idx) ||
+      !is_device_ptr(topk_logit) || !is_device_ptr(workspace))
+    return KD_ERR_INVALID_ARG;
+  const CachePlan p = make_cache_plan(N, V, chunk);
+  if (workspace_bytes < p.total) return KD_ERR_OOM;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  prof().used = 0;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  DevStatus* dst = reinterpret_cast<DevStatus*>(base + p.off_status);
+  float2* part = reinterpret_cast<float2*>(base + p.off_part);
+  float* zbuf = reinterpret_cast<float*>(base + p.off_z);
+
+  const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap tm_hid_k, tm_w_k, tm_z_st;
+  bool ok = true;
+  ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
+  ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, b_box_rows(kd::GV_FWDZ));
+  ok &= make_map(&tm_z_st, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, zbuf, V, p.chunk, 32, 32);
+  if (!ok) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed");
+    return KD_ERR_CUDA;
+  }
+  KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
+  for (int j = 0; j < p.n_chunks; ++j) {
+    const int row0 = j * p.chunk;
+    const int cj = static_cast<int>(std::min<long long>(p.chunk, N - row0));
+    kd::GemmArgs g{};
+    g.m_tiles = static_cast<int>(cdiv(cj, kd::gemm_tile_m(kd::GV_FWDZ)));
+    g.n_tiles = p.vt; g.splits = 1;
+    g.kb_total = static_cast<int>(cdiv(H, 64));
+    g.order = kd::ORDER_M_FAST; g.a_row0 = row0; g.b_row0 = 0;
+    g.timeout_ns = kDefaultTimeoutNs; g.status = dst;
+    kd::EpiArgs e{};
+    // the forward epilogue with scale 1 and no cached ids: part[.].x is the
+    // exact maximum of each (row, 256-wide vocab tile), z is stored in fp32
+    e.rows_valid = cj; e.cols_valid = V; e.scale2 = 1.f; e.alpha = 1.f;
+    e.K = 0; e.grow0 = row0; e.c_alloc = p.chunk; e.part = part;
+    { ProfScope ps_(PK_CACHE_GEMM, s);
+      KD_CUDA(kd::launch_gemm(kd::GV_FWDZ, tm_hid_k, tm_w_k, tm_z_st, g, e, s)); }
+    { ProfScope ps_(PK_CACHE_SELECT, s);
+      KD_CUDA(kd::launch_topk_select(zbuf, V, part, p.vt, p.chunk, cj, K, row0, topk_idx,
+                                     topk_logit, s)); }
+  }
+  DevStatus hs{};
+  KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+  KD_CUDA(cudaStreamSynchronize(s));
+  prof_collect();
   if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
   return KD_OK;
 }

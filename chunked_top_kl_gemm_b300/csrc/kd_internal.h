@@ -68,6 +68,13 @@ cudaError_t launch_dz_from_z(const float* z, int V, int rows_valid, int rows_cov
                              const float* lse2, float scale2, const uint8_t* mask, int grow0,
                              const int* sid, const float* sp, int K, void* dz, cudaStream_t s);
 
+// Top-K cache rows [0, rows_valid) of a chunk from its stored logits z
+// [rows][V] and per-tile maxima part[n_tiles][c_alloc].x, written to rows
+// row0.. of out_idx / out_val [N][K].  K <= 8192.
+cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_tiles,
+                               int c_alloc, int rows_valid, int K, long long row0,
+                               int32_t* out_idx, float* out_val, cudaStream_t s);
+
 cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStatus* st,
                               cudaStream_t s);
 

@@ -509,6 +509,185 @@ cudaError_t launch_dz_from_z(const float* z, int V, int rows_valid, int rows_cov
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ top-K cache select
+// Offline teacher cache: per row of a chunk's stored fp32 logits z [rows][V],
+// the K largest values in decreasing order with equal values ordered by
+// increasing id.  Values are compared through an order-preserving 32-bit key;
+// a candidate is the 64-bit (key << 32 | ~id), so sorting candidates in
+// decreasing order sorts by value, then by increasing id.
+//
+// Fast path: the K-th largest of the row's per-tile maxima (from the GEMM
+// epilogue) is a lower bound of its K-th largest value, since K tiles hold a
+// value at least that large; one pass collects every value at or above it
+// (typically about K of them) and a bitonic sort orders them.  Exact path,
+// when the candidates overflow shared memory (or K exceeds the tile count):
+// a three-pass radix select finds the K-th largest key, then the larger keys
+// and, in increasing id order, enough of the equal keys are gathered.
+constexpr int SEL_THREADS = 512;
+constexpr int SEL_CAP = 8192;          // candidates a block holds (>= K)
+constexpr int SEL_BINS = 2048;
+
+__device__ __forceinline__ uint32_t sel_key(float f) {
+  const uint32_t b = __float_as_uint(f + 0.0f);      // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float sel_val(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ unsigned long long sel_cand(uint32_t key, int id) {
+  return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~id);
+}
+
+// Sort s[0..P) (P a power of two) in decreasing order; all threads call.
+__device__ void sel_bitonic_desc(unsigned long long* s, int P) {
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += SEL_THREADS) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = s[i], b = s[ixj];
+          const bool first_half = (i & k) == 0;
+          if (first_half ? (a < b) : (a > b)) { s[i] = b; s[ixj] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(SEL_THREADS) kd_topk_select(
+    const float* __restrict__ z, int V, const float2* __restrict__ part, int n_tiles,
+    int c_alloc, int K, long long row0, int32_t* __restrict__ out_idx, float* __restrict__ out_val) {
+  extern __shared__ unsigned long long cand[];                    // [SEL_CAP]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(cand + SEL_CAP);    // [SEL_BINS]
+  uint32_t* scan = hist + SEL_BINS;                                 // [SEL_THREADS]
+  __shared__ uint32_t s_cnt, s_prefix, s_rank;
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const float* zr = z + static_cast<long long>(r) * V;
+  auto pow2 = [](int n) { int p = 1; while (p < n) p <<= 1; return p; };
+
+  // 1) lower bound of the K-th largest value: the K-th largest tile maximum
+  float tau0 = -CUDART_INF_F;
+  if (K <= n_tiles && n_tiles <= SEL_CAP) {
+    const int P = pow2(n_tiles);
+    for (int t = tid; t < P; t += SEL_THREADS)
+      cand[t] = t < n_tiles ? sel_cand(sel_key(part[static_cast<long long>(t) * c_alloc + r].x), t)
+                            : 0ull;
+    __syncthreads();
+    sel_bitonic_desc(cand, P);
+    tau0 = sel_val(static_cast<uint32_t>(cand[K - 1] >> 32));
+    __syncthreads();
+  }
+
+  // 2) every value >= tau0 (at least K of them)
+  if (tid == 0) s_cnt = 0;
+  __syncthreads();
+  for (int v = tid * 4; v < V; v += SEL_THREADS * 4) {
+    const float4 x = *reinterpret_cast<const float4*>(zr + v);
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (xs[c] >= tau0) {
+        const uint32_t slot = atomicAdd(&s_cnt, 1u);
+        if (slot < SEL_CAP) cand[slot] = sel_cand(sel_key(xs[c]), v + c);
+      }
+    }
+  }
+  __syncthreads();
+  int n = static_cast<int>(s_cnt);
+
+  if (n > SEL_CAP) {
+    // 3) exact K-th largest key by radix select (11 + 11 + 10 bits)
+    uint32_t prefix = 0, pmask = 0, kk = static_cast<uint32_t>(K);
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sh = shifts[pass], nb = 1 << widths[pass];
+      for (int b = tid; b < nb; b += SEL_THREADS) hist[b] = 0;
+      __syncthreads();
+      for (int v = tid; v < V; v += SEL_THREADS) {
+        const uint32_t key = sel_key(zr[v]);
+        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t above = 0;
+        int b = nb - 1;
+        for (; b > 0; --b) {
+          if (above + hist[b] >= kk) break;
+          above += hist[b];
+        }
+        s_prefix = prefix | (static_cast<uint32_t>(b) << sh);
+        s_rank = kk - above;
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      kk = s_rank;
+      pmask |= static_cast<uint32_t>(nb - 1) << sh;
+      __syncthreads();
+    }
+    const uint32_t tau = prefix;                   // the K-th largest key
+    const int need = static_cast<int>(kk);         // equal keys to take
+    // 4) the keys above tau (fewer than K)
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    for (int v = tid; v < V; v += SEL_THREADS) {
+      const uint32_t key = sel_key(zr[v]);
+      if (key > tau) cand[atomicAdd(&s_cnt, 1u)] = sel_cand(key, v);
+    }
+    __syncthreads();
+    const int n_gt = static_cast<int>(s_cnt);
+    // 5) the `need` lowest ids among the keys equal to tau: each thread scans
+    // a contiguous id range; an exclusive scan of the counts orders them
+    const int L = (V + SEL_THREADS - 1) / SEL_THREADS;
+    const int v0 = tid * L, v1 = min(V, v0 + L);
+    uint32_t mine = 0;
+    for (int v = v0; v < v1; ++v) mine += sel_key(zr[v]) == tau;
+    scan[tid] = mine;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t acc = 0;
+      for (int i = 0; i < SEL_THREADS; ++i) { const uint32_t c = scan[i]; scan[i] = acc; acc += c; }
+    }
+    __syncthreads();
+    uint32_t rank = scan[tid];
+    for (int v = v0; v < v1 && rank < static_cast<uint32_t>(need); ++v) {
+      if (sel_key(zr[v]) == tau) { cand[n_gt + rank] = sel_cand(tau, v); ++rank; }
+    }
+    __syncthreads();
+    n = K;
+  }
+
+  // 6) order the candidates and write the first K
+  const int P = pow2(n);
+  for (int i = n + tid; i < P; i += SEL_THREADS) cand[i] = 0ull;
+  __syncthreads();
+  sel_bitonic_desc(cand, P);
+  const long long o = (row0 + r) * static_cast<long long>(K);
+  for (int k = tid; k < K; k += SEL_THREADS) {
+    const unsigned long long c = cand[k];
+    out_val[o + k] = sel_val(static_cast<uint32_t>(c >> 32));
+    out_idx[o + k] = static_cast<int32_t>(~static_cast<uint32_t>(c));
+  }
+}
+
+cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_tiles,
+                               int c_alloc, int rows_valid, int K, long long row0,
+                               int32_t* out_idx, float* out_val, cudaStream_t s) {
+  const size_t smem = SEL_CAP * sizeof(unsigned long long) + (SEL_BINS + SEL_THREADS) * 4;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kd_topk_select,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kd_topk_select<<<rows_valid, SEL_THREADS, smem, s>>>(z, V, part, n_tiles, c_alloc, K, row0,
+                                                       out_idx, out_val);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ token mask
 // n_valid = number of tokens whose mask byte is nonzero; alpha = 1/(T n_valid)
 // (0 when no token is valid), the gradient scale of a masked call.

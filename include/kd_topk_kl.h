@@ -170,6 +170,31 @@ kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int3
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The offline top-K teacher cache (the step before the loss): per token,
+ * the teacher's K highest logits and their ids, computed once and stored
+ * (epoka.news, "The two proposed changes"; glonce.com, body;
+ * ainewsbank.com, "Two changes remove different bottlenecks": K = 100).
+ *
+ *   hidden      bf16 [N, H]  teacher final hidden states (device)
+ *   W           bf16 [V, H]  teacher LM head, z = hidden W^T (device)
+ *   K           1 <= K <= min(V, 8192)
+ *   chunk       token rows per chunk (rounded up to a multiple of 128); the
+ *               workspace holds one chunk's fp32 logits (chunk x V x 4 bytes)
+ *   topk_idx    int32 [N, K] out (device): ids in decreasing logit order,
+ *               equal logits in increasing id order (the pages leave ties open)
+ *   topk_logit  fp32 [N, K] out (device): the logits z (fp32 accumulation of
+ *               the bf16 products), decreasing
+ * The logits are computed on the tensor cores one chunk at a time; the
+ * selection is exact for those fp32 values.  Same pointer, error and
+ * synchronisation rules as kd_topk_kl_fwd_bwd_ex; the caller owns the
+ * workspace (kd_topk_cache_workspace_size bytes, 256-byte aligned).
+ */
+size_t kd_topk_cache_workspace_size(int64_t N, int H, int V, int K, int chunk);
+kd_status kd_topk_cache_build(const void* hidden, const void* W, int64_t N, int H, int V, int K,
+                              int chunk, int32_t* topk_idx, float* topk_logit, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * Test and diagnosis options for kd_topk_kl_debug.  Each output pointer may
  * be NULL (not written).
  *   lse        fp32 [N]    logsumexp_v(z_n / T) (device)
