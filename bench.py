@@ -438,6 +438,64 @@ def run_sweep(args):
         del inp, gh, gW, ws, args_
 
 
+# ------------------------------------------------------------------ cache builder
+def run_cache_build(args):
+    """Throughput of the offline top-K cache builder on the workload's head
+    (the teacher side: hidden [N,H] through W [V,H], K per token)."""
+    import torch
+
+    import chunked_top_kl_gemm_b300 as kd
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kd.lib()
+    cfg = workloads.CONFIGS[args.config]
+    chunk = args.chunk or cfg.chunk
+    N, H, V, K = cfg.N, cfg.H, cfg.V, cfg.K
+    inp = workloads.make_inputs(cfg, seed=0, device=dev)
+    h, W = inp["hidden"], inp["W"]
+    idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    val = torch.empty((N, K), dtype=torch.float32, device=dev)
+    ws = torch.empty(kd.kd_topk_cache_workspace_size(N, H, V, K, chunk), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        kd.kd_topk_cache_build(h, W, K, chunk, topk_idx=idx, topk_logit=val, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    kd.kd_profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    kd.kd_profile_enable(False)
+    prof = kd.kd_profile_read()
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    peaks, _ = load_peaks()
+    gemm_ms = prof["cache_gemm_logits"][0] / args.steps
+    sel_ms = prof["cache_topk_select"][0] / args.steps
+    # the select reads every stored logit once (4 N V bytes) on its fast path
+    print(json.dumps({
+        "metric": "tokens/s offline top-K cache build (N x H x V GEMM + top-K select)",
+        "value": N / t, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "N": N, "H": H, "V": V, "K": K, "chunk": chunk},
+        "gemm_tflops": 2.0 * N * H * V / (gemm_ms / 1e3) / 1e12,
+        "gemm_frac_bf16_peak_burst": 2.0 * N * H * V / (gemm_ms / 1e3) / 1e12
+                                     / float(peaks["bf16_tflops"]),
+        "select_gbs": 4.0 * N * V / (sel_ms / 1e3) / 1e9,
+        "select_frac_hbm": 4.0 * N * V / (sel_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+        "kernels": {k: {"ms_per_step": v[0] / args.steps} for k, v in prof.items() if v[1]},
+    }), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,9 +516,13 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="peak memory and throughput over token counts and chunk sizes "
                          "(one JSON line per point)")
+    ap.add_argument("--cache-build", action="store_true",
+                    help="time the offline top-K cache builder on the workload's head")
     args = ap.parse_args(argv)
     if args.sweep:
         return run_sweep(args)
+    if args.cache_build:
+        return run_cache_build(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
