@@ -566,32 +566,55 @@ __global__ void __launch_bounds__(SEL_THREADS) kd_topk_select(
   const float* zr = z + static_cast<long long>(r) * V;
   auto pow2 = [](int n) { int p = 1; while (p < n) p <<= 1; return p; };
 
-  // 1) lower bound of the K-th largest value: the K-th largest tile maximum
-  float tau0 = -CUDART_INF_F;
-  if (K <= n_tiles && n_tiles <= SEL_CAP) {
-    const int P = pow2(n_tiles);
-    for (int t = tid; t < P; t += SEL_THREADS)
-      cand[t] = t < n_tiles ? sel_cand(sel_key(part[static_cast<long long>(t) * c_alloc + r].x), t)
-                            : 0ull;
+  // 1) lower bound of the K-th largest value: the K-th largest tile maximum.
+  // Tile maximum i is the K-th largest when exactly K - 1 others precede it
+  // in (value descending, index ascending) order.
+  __shared__ float s_tau0;
+  if (tid == 0) s_tau0 = -CUDART_INF_F;
+  float* tmax = reinterpret_cast<float*>(cand);
+  if (K <= n_tiles && n_tiles <= 2 * SEL_CAP) {
+    for (int t = tid; t < n_tiles; t += SEL_THREADS)
+      tmax[t] = part[static_cast<long long>(t) * c_alloc + r].x + 0.0f;
     __syncthreads();
-    sel_bitonic_desc(cand, P);
-    tau0 = sel_val(static_cast<uint32_t>(cand[K - 1] >> 32));
-    __syncthreads();
+    for (int i = tid; i < n_tiles; i += SEL_THREADS) {
+      const float mi = tmax[i];
+      int before = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const float mj = tmax[j];
+        before += (mj > mi) || (mj == mi && j < i);
+      }
+      if (before == K - 1) s_tau0 = mi;
+    }
   }
-
-  // 2) every value >= tau0 (at least K of them)
   if (tid == 0) s_cnt = 0;
   __syncthreads();
-  for (int v = tid * 4; v < V; v += SEL_THREADS * 4) {
-    const float4 x = *reinterpret_cast<const float4*>(zr + v);
-    const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (xs[c] >= tau0) {
-        const uint32_t slot = atomicAdd(&s_cnt, 1u);
-        if (slot < SEL_CAP) cand[slot] = sel_cand(sel_key(xs[c]), v + c);
-      }
+  const float tau0 = s_tau0;
+
+  // 2) every value >= tau0 (at least K of them); four 16-byte streaming
+  // loads in flight per thread
+  auto take = [&](float x, int id) {
+    if (x >= tau0) {
+      const uint32_t slot = atomicAdd(&s_cnt, 1u);
+      if (slot < SEL_CAP) cand[slot] = sel_cand(sel_key(x), id);
     }
+  };
+  const float4* z4 = reinterpret_cast<const float4*>(zr);
+  const int V4 = V >> 2;
+  int i4 = tid;
+  for (; i4 + 3 * SEL_THREADS < V4; i4 += 4 * SEL_THREADS) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = __ldcs(z4 + i4 + u * SEL_THREADS);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = (i4 + u * SEL_THREADS) * 4;
+      take(x[u].x, v); take(x[u].y, v + 1); take(x[u].z, v + 2); take(x[u].w, v + 3);
+    }
+  }
+  for (; i4 < V4; i4 += SEL_THREADS) {
+    const float4 x = __ldcs(z4 + i4);
+    const int v = i4 * 4;
+    take(x.x, v); take(x.y, v + 1); take(x.z, v + 2); take(x.w, v + 3);
   }
   __syncthreads();
   int n = static_cast<int>(s_cnt);
