@@ -47,18 +47,25 @@ def load_peaks() -> tuple:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("kd_args.h", "kd_gemm.cuh", "kd_internal.h", "kd_kernels.cu", "kd_ptx.cuh")
+GEMM_SOURCES = ("kd_args.h", "kd_gemm.cuh", "kd_ptx.cuh")
+GEMM_SECTION_END = b"// ------------------------------------------------------------------ prep"
 
 
 def kernel_source_hash() -> str:
-    """Hash of the device-code sources (kernels, their arguments and launch
-    helpers), to tell whether stored counters are current."""
+    """Hash of the sources that define the GEMM kernels: their template, PTX
+    helpers and arguments, and the part of kd_kernels.cu that instantiates
+    and launches them (up to the first SIMT kernel).  Stored DRAM counters
+    are reported only while this hash is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_top_kl_gemm_b300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in GEMM_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
+    with open(os.path.join(csrc, "kd_kernels.cu"), "rb") as f:
+        text = f.read()
+    h.update(b"kd_kernels.cu")
+    h.update(text.split(GEMM_SECTION_END)[0])
     return h.hexdigest()[:16]
 
 
