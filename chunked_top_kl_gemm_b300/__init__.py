@@ -310,7 +310,7 @@ def kd_gemm_bf16_test(A, B, a_mn: bool, b_mn: bool, bn: int = 0, pair: bool = Fa
         raise ValueError("K mismatch")
     C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     st = lib().kd_gemm_bf16_test(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(bool(a_mn)),
-                                 int(bool(b_mn)), int(bn), int(bool(pair)),
+                                 int(bool(b_mn)), int(bn), int(pair),
                                  _stream_handle(stream))
     _check(st, "kd_gemm_bf16_test")
     return C

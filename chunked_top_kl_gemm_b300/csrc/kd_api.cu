@@ -502,7 +502,10 @@ kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int variant = a_mn ? (b_mn ? kd::GV_TEST_MM : kd::GV_TEST_MK)
                      : (b_mn ? kd::GV_TEST_KM : kd::GV_TEST_KK);
-  if (pair) {
+  if (pair == 2) {
+    if ((bn != 0 && bn != 256) || a_mn || b_mn) return KD_ERR_INVALID_ARG;
+    variant = kd::GV_TEST_KK2S;
+  } else if (pair) {
     if (bn != 0 && bn != 256) return KD_ERR_INVALID_ARG;
     variant = a_mn ? (b_mn ? kd::GV_TEST_MM2 : kd::GV_TEST_MK2)
                    : (b_mn ? kd::GV_TEST_KM2 : kd::GV_TEST_KK2);

@@ -45,7 +45,8 @@ constexpr int EPI_WARP0 = 2;
 constexpr int EPI_THREADS = 128;
 constexpr int EPI_STAGE_BYTES = 4096;   // one 32-row x 128-byte staging box
 
-template <int BN_, bool A_MN_, bool B_MN_, int STAGES_, int KIND_, bool CTA2_ = false>
+template <int BN_, bool A_MN_, bool B_MN_, int STAGES_, int KIND_, bool CTA2_ = false,
+          int KSUB_ = 1>
 struct GemmCfg {
   static constexpr int BN = BN_;           // N of one accumulator tile (both CTAs of a pair)
   static constexpr bool A_MN = A_MN_;
@@ -56,8 +57,11 @@ struct GemmCfg {
   static constexpr int NCTA = CTA2 ? 2 : 1;
   static constexpr int TILE_M = BM * NCTA; // M of one work unit
   static constexpr int BN_CTA = BN / NCTA; // B rows one CTA loads and holds
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN_CTA * BK * 2;
+  static constexpr int KSUB = KSUB_;       // 64-deep k-blocks per ring stage
+  static constexpr int A_SUB = BM * BK * 2;          // one k-block of A
+  static constexpr int B_SUB = BN_CTA * BK * 2;      // one k-block of B
+  static constexpr int A_BYTES = KSUB * A_SUB;       // one stage
+  static constexpr int B_BYTES = KSUB * B_SUB;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TX_BYTES = NCTA * STAGE_BYTES;   // one stage of the whole pair
   static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
@@ -222,42 +226,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int a_m0 = t.m * C::TILE_M + static_cast<int>(rank) * BM;
         const int b_n0 = t.n * C::BN + static_cast<int>(rank) * (tile_cols(t.n) / C::NCTA);
         bool ok = true;
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; kb += C::KSUB) {
           if (*abort_word || !mbar_wait(&empty[stage], phase ^ 1u, w, SITE_PROD)) { ok = false; break; }
-          uint8_t* a = sA + stage * C::A_BYTES;
-          uint8_t* b = sB + stage * C::B_BYTES;
-          const int k0 = kb * BK;
-          if constexpr (!C::CTA2) {
-            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            if (!C::A_MN) {
-              tma_load_2d(a, &tmA, &full[stage], k0, g.a_row0 + a_m0);
-            } else {
-              tma_load_2d(a, &tmA, &full[stage], a_m0, g.a_row0 + k0);
-              tma_load_2d(a + 8192, &tmA, &full[stage], a_m0 + 64, g.a_row0 + k0);
-            }
-            if (!C::B_MN) {
-              tma_load_2d(b, &tmB, &full[stage], k0, g.b_row0 + b_n0);
-            } else {
+          // a stage always carries KSUB k-blocks (the byte count stays fixed); a
+          // k-block past the unit's end is loaded but not multiplied
+          if constexpr (!C::CTA2) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          else if (leader) mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
+          const uint32_t fb = C::CTA2 ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
 #pragma unroll
-              for (int j = 0; j < C::BN_CTA / 64; ++j)
-                tma_load_2d(b + j * 8192, &tmB, &full[stage], b_n0 + j * 64, g.b_row0 + k0);
-            }
-          } else {
-            // both CTAs' bytes complete on the leader's full barrier
-            if (leader) mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
-            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-            if (!C::A_MN) {
-              tma_load_2d_pair(a, &tmA, fb, k0, g.a_row0 + a_m0);
-            } else {
-              tma_load_2d_pair(a, &tmA, fb, a_m0, g.a_row0 + k0);
-              tma_load_2d_pair(a + 8192, &tmA, fb, a_m0 + 64, g.a_row0 + k0);
-            }
-            if (!C::B_MN) {
-              tma_load_2d_pair(b, &tmB, fb, k0, g.b_row0 + b_n0);
-            } else {
+          for (int j = 0; j < C::KSUB; ++j) {
+            uint8_t* a = sA + stage * C::A_BYTES + j * C::A_SUB;
+            uint8_t* b = sB + stage * C::B_BYTES + j * C::B_SUB;
+            const int k0 = (kb + j) * BK;
+            if constexpr (!C::CTA2) {
+              if (!C::A_MN) {
+                tma_load_2d(a, &tmA, &full[stage], k0, g.a_row0 + a_m0);
+              } else {
+                tma_load_2d(a, &tmA, &full[stage], a_m0, g.a_row0 + k0);
+                tma_load_2d(a + 8192, &tmA, &full[stage], a_m0 + 64, g.a_row0 + k0);
+              }
+              if (!C::B_MN) {
+                tma_load_2d(b, &tmB, &full[stage], k0, g.b_row0 + b_n0);
+              } else {
 #pragma unroll
-              for (int j = 0; j < C::BN_CTA / 64; ++j)
-                tma_load_2d_pair(b + j * 8192, &tmB, fb, b_n0 + j * 64, g.b_row0 + k0);
+                for (int jj = 0; jj < C::BN_CTA / 64; ++jj)
+                  tma_load_2d(b + jj * 8192, &tmB, &full[stage], b_n0 + jj * 64, g.b_row0 + k0);
+              }
+            } else {
+              // both CTAs' bytes complete on the leader's full barrier
+              if (!C::A_MN) {
+                tma_load_2d_pair(a, &tmA, fb, k0, g.a_row0 + a_m0);
+              } else {
+                tma_load_2d_pair(a, &tmA, fb, a_m0, g.a_row0 + k0);
+                tma_load_2d_pair(a + 8192, &tmA, fb, a_m0 + 64, g.a_row0 + k0);
+              }
+              if (!C::B_MN) {
+                tma_load_2d_pair(b, &tmB, fb, k0, g.b_row0 + b_n0);
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < C::BN_CTA / 64; ++jj)
+                  tma_load_2d_pair(b + jj * 8192, &tmB, fb, b_n0 + jj * 64, g.b_row0 + k0);
+              }
             }
           }
           ++issued;
@@ -283,6 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t b_desc0 = C::B_MN ? sdesc_sw128(smem_u32(sB), 8192, 1024)
                                        : sdesc_sw128(smem_u32(sB), 16, 1024);
       constexpr uint32_t A_STEP = C::A_BYTES >> 4, B_STEP = C::B_BYTES >> 4;
+      constexpr uint32_t A_SUBD = C::A_SUB >> 4, B_SUBD = C::B_SUB >> 4;
       constexpr uint32_t A_KK = C::A_MN ? (2048 >> 4) : (32 >> 4);   // one UMMA_K slice
       constexpr uint32_t B_KK = C::B_MN ? (2048 >> 4) : (32 >> 4);
       uint64_t a_desc = a_desc0, b_desc = b_desc0;
@@ -297,12 +307,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int nn = tile_cols(t.n);
         const uint32_t idesc_t = idesc_bf16(C::TILE_M, nn, C::A_MN, C::B_MN);
         uint32_t first = 0;   // the unit's first MMA overwrites the accumulator
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; kb += C::KSUB) {
           if (!mbar_wait(&full[stage], phase, w, SITE_MMA_FULL)) { ok = false; break; }
           tc_mma_bf16<C::NCTA>(d, a_desc, b_desc, idesc_t, first);
 #pragma unroll
           for (int kk = 1; kk < BK / UMMA_K; ++kk)
             tc_mma_bf16_acc<C::NCTA>(d, a_desc + kk * A_KK, b_desc + kk * B_KK, idesc_t);
+#pragma unroll
+          for (int j = 1; j < C::KSUB; ++j) {
+            if (kb + j < t.kb1) {
+#pragma unroll
+              for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                tc_mma_bf16_acc<C::NCTA>(d, a_desc + j * A_SUBD + kk * A_KK,
+                                         b_desc + j * B_SUBD + kk * B_KK, idesc_t);
+            }
+          }
           first = 1;
           if constexpr (C::CTA2) tc_commit_pair(&empty[stage]);
           else tc_commit<1>(&empty[stage]);

@@ -30,6 +30,7 @@ enum GemmVariant {
   GV_TEST_MK2 = 14,
   GV_TEST_MM2 = 15,
   GV_FWDZ = 16,        // K1 that also stores the chunk's fp32 logits
+  GV_TEST_KK2S = 17,   // pair, K-major operands, two k-blocks per ring stage
 };
 
 // Tile width of the N dimension of each variant.

@@ -35,12 +35,15 @@ namespace kd {
 
 // The loss's GEMMs run on CTA pairs (2-CTA MMA, 256 x 256 tiles): per SM
 // they pull 32 KB of operands from L2 per 64-deep k-block instead of 48 KB.
-using CfgFwd = GemmCfg<256, false, false, 7, EPI_FWD, true>;
-using CfgDz = GemmCfg<256, false, false, 6, EPI_DZ, true>;
+// FWD and DZ stream L2-resident operands and are bound by the MMA issue:
+// two 64-deep k-blocks per ring stage halve the issuer's waits and commits.
+// The gradient GEMMs wait on DRAM-fed operands and keep finer stages.
+using CfgFwd = GemmCfg<256, false, false, 3, EPI_FWD, true, 2>;
+using CfgDz = GemmCfg<256, false, false, 3, EPI_DZ, true, 2>;
 using CfgGradH = GemmCfg<256, true, false, 6, EPI_F32, true>;   // grad_hidden^T = W^T dZ^T
 using CfgGradW = GemmCfg<256, true, false, 6, EPI_ACC, true>;   // grad_W = dZ^T h_c
 // forward that also keeps the chunk's fp32 logits (backward without recompute)
-using CfgFwdZ = GemmCfg<256, false, false, 6, EPI_FWDZ, true>;
+using CfgFwdZ = GemmCfg<256, false, false, 3, EPI_FWDZ, true, 2>;
 // single-CTA forms (128 x BN tiles), kept for the GEMM-core tests
 using CfgTestKK = GemmCfg<256, false, false, 4, EPI_F32>;
 using CfgTestKM = GemmCfg<192, false, true, 4, EPI_F32>;
@@ -55,6 +58,8 @@ using CfgTestKK2 = GemmCfg<256, false, false, 6, EPI_F32, true>;
 using CfgTestKM2 = GemmCfg<256, false, true, 6, EPI_F32, true>;
 using CfgTestMK2 = GemmCfg<256, true, false, 6, EPI_F32, true>;
 using CfgTestMM2 = GemmCfg<256, true, true, 6, EPI_F32, true>;
+// pair form with two k-blocks per stage (the FWD / DZ ring)
+using CfgTestKK2S = GemmCfg<256, false, false, 3, EPI_F32, true, 2>;
 
 // Work units that can run at once: one per SM, or one per co-resident CTA
 // pair (queried once per instantiation).
@@ -136,7 +141,7 @@ static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const 
   X(GV_TEST_MM, CfgTestMM) X(GV_TEST_KK192, CfgTestKK192) X(GV_TEST_KM256, CfgTestKM256) \
   X(GV_TEST_MK256, CfgTestMK256) X(GV_TEST_MM256, CfgTestMM256)                         \
   X(GV_TEST_KK2, CfgTestKK2) X(GV_TEST_KM2, CfgTestKM2) X(GV_TEST_MK2, CfgTestMK2)       \
-  X(GV_TEST_MM2, CfgTestMM2) X(GV_FWDZ, CfgFwdZ)
+  X(GV_TEST_MM2, CfgTestMM2) X(GV_FWDZ, CfgFwdZ) X(GV_TEST_KK2S, CfgTestKK2S)
 
 int gemm_bn(int variant) {
 #define X(V, C) case V: return C::BN;

@@ -235,7 +235,9 @@ kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* top
  * pair == 0: one CTA per 128 x bn tile, bn the tile width of the N dimension
  * (192 or 256; 0 = the default of this layout).  pair != 0: a CTA pair per
  * 256 x 256 tile with 2-CTA MMAs, the form the loss's GEMMs use (bn 0 or
- * 256).  M, N, K multiples of 8; all pointers device, 16-byte aligned.
+ * 256); pair == 2: the same with two 64-deep k-blocks per pipeline stage
+ * (K-major A and B only).  M, N, K multiples of 8; all pointers device,
+ * 16-byte aligned.
  * Synchronises `stream` before returning.
  */
 kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N, int K, int a_mn,

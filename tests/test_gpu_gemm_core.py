@@ -50,6 +50,21 @@ def test_gemm_layouts_cta_pair(a_mn, b_mn, M, N, K):
     assert err < 1e-5, err
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (136, 264, 72), (392, 520, 136),
+                                   (1000, 2880, 200), (512, 768, 2880)])
+def test_gemm_cta_pair_two_kblocks_per_stage(M, N, K):
+    """The FWD / DZ ring: two 64-deep k-blocks per stage, odd k-block counts
+    included (the stage's second k-block is then loaded but not multiplied)."""
+    ensure_lib()
+    g = torch.Generator().manual_seed(M + 3 * N + 7 * K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    C = kd.kd_gemm_bf16_test(A.cuda(), B.cuda(), False, False, 0, pair=2).cpu().double().numpy()
+    ref = A.double().numpy() @ B.double().numpy().T
+    err = np.abs(C - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, err
+
+
 def test_gemm_cta_pair_is_deterministic_and_matches_single_cta():
     ensure_lib()
     g = torch.Generator().manual_seed(3)
