@@ -221,13 +221,21 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_
   return p;
 }
 
+// Device memory of the current device, or managed memory.
 bool is_device_ptr(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();  // clear the sticky-free error of an unknown pointer
     return false;
   }
-  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+  if (a.type == cudaMemoryTypeManaged) return true;
+  if (a.type != cudaMemoryTypeDevice) return false;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.device == dev;
 }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -252,10 +260,10 @@ kd_status validate(const void* hidden, const void* W, const int32_t* idx, const 
 // zero gradient rows.  flags: KD_FLAG_ACCUMULATE adds into grad_hidden /
 // grad_W; KD_FLAG_STORE_LOGITS keeps each chunk's fp32 logits from the
 // forward GEMM and forms dZ from them instead of recomputing the GEMM.
-kd_status run(const void* hidden, const void* W, const int32_t* idx, const float* logit,
-              long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
-              float* gW, void* ws, size_t ws_bytes, cudaStream_t s, const kd_debug_opts* opts,
-              const uint8_t* mask = nullptr, unsigned flags = 0) {
+kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const float* logit,
+                   long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
+                   float* gW, void* ws, size_t ws_bytes, cudaStream_t s,
+                   const kd_debug_opts* opts, const uint8_t* mask, unsigned flags) {
   const int accumulate = (flags & KD_FLAG_ACCUMULATE) ? 1 : 0;
   const bool store_z = (flags & KD_FLAG_STORE_LOGITS) != 0;
   if (flags & ~(KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS)) return KD_ERR_INVALID_ARG;
@@ -407,6 +415,22 @@ kd_status run(const void* hidden, const void* W, const int32_t* idx, const float
   const long long n_mean = mask ? hs.n_valid : N;
   *loss = n_mean > 0 ? static_cast<float>(hs.loss_sum / static_cast<double>(n_mean)) : 0.f;
   return KD_OK;
+}
+
+// run_impl, and after a CUDA error part-way through the chunk loop, a
+// best-effort synchronisation: the call never returns while its own kernels
+// may still use the caller's workspace or outputs.
+kd_status run(const void* hidden, const void* W, const int32_t* idx, const float* logit,
+              long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
+              float* gW, void* ws, size_t ws_bytes, cudaStream_t s, const kd_debug_opts* opts,
+              const uint8_t* mask = nullptr, unsigned flags = 0) {
+  const kd_status st = run_impl(hidden, W, idx, logit, N, H, V, K, T, chunk, loss, gh, gW, ws,
+                                ws_bytes, s, opts, mask, flags);
+  if (st == KD_ERR_CUDA) {
+    cudaStreamSynchronize(s);
+    cudaGetLastError();
+  }
+  return st;
 }
 
 }  // namespace
@@ -573,18 +597,9 @@ bool cache_sizes_ok(long long N, int H, int V, int K, int chunk) {
          K >= 1 && K <= V && K <= 8192 && chunk >= 1;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t kd_topk_cache_workspace_size(int64_t N, int H, int V, int K, int chunk) {
-  if (!cache_sizes_ok(N, H, V, K, chunk)) return 0;
-  return make_cache_plan(N, V, chunk).total;
-}
-
-kd_status kd_topk_cache_build(const void* hidden, const void* W, int64_t N, int H, int V, int K,
-                              int chunk, int32_t* topk_idx, float* topk_logit, void* workspace,
-                              size_t workspace_bytes, void* stream) {
+kd_status cache_build_impl(const void* hidden, const void* W, int64_t N, int H, int V, int K,
+                           int chunk, int32_t* topk_idx, float* topk_logit, void* workspace,
+                           size_t workspace_bytes, void* stream) {
   if (!hidden || !W || !topk_idx || !topk_logit || !workspace) return KD_ERR_INVALID_ARG;
   if (!cache_sizes_ok(N, H, V, K, chunk)) return KD_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(topk_idx, 4) ||
@@ -639,6 +654,27 @@ kd_status kd_topk_cache_build(const void* hidden, const void* W, int64_t N, int 
   prof_collect();
   if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
   return KD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kd_topk_cache_workspace_size(int64_t N, int H, int V, int K, int chunk) {
+  if (!cache_sizes_ok(N, H, V, K, chunk)) return 0;
+  return make_cache_plan(N, V, chunk).total;
+}
+
+kd_status kd_topk_cache_build(const void* hidden, const void* W, int64_t N, int H, int V, int K,
+                              int chunk, int32_t* topk_idx, float* topk_logit, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  const kd_status st = cache_build_impl(hidden, W, N, H, V, K, chunk, topk_idx, topk_logit,
+                                        workspace, workspace_bytes, stream);
+  if (st == KD_ERR_CUDA) {   // never return while its kernels may still run
+    cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    cudaGetLastError();
+  }
+  return st;
 }
 
 }  // extern "C"

@@ -36,11 +36,16 @@
  * unregistered pointers are rejected with KD_ERR_INVALID_ARG before any
  * launch.  All arrays are dense and row-major.
  *
+ * Pointers to device memory must belong to the current device (managed
+ * memory is accepted too).
+ *
  * Errors.  Argument errors are detected on the host before anything is
  * launched.  Device-side errors (an id outside [0, V), a bounded wait that
  * ran out) are reported after the stream has been synchronised; on any
  * error the outputs are unspecified.  Every call returns after a stream
- * synchronisation, because `loss` is a host pointer.
+ * synchronisation (also after a CUDA error part-way through), because
+ * `loss` is a host pointer: when it returns, none of its kernels still uses
+ * the workspace or the outputs.
  *
  * Thread safety.  Calls on different streams may run concurrently if they
  * use different workspaces.
