@@ -175,6 +175,40 @@ def throughput(tokens_per_rank: int, steps: int, world: int, seconds: float) -> 
 
 
 # ------------------------------------------------------------------ oracle legs
+def host_info() -> dict:
+    """CPU model and BLAS library of the host the oracle runs on."""
+    info = {"cpu_model": None, "blas": None}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    info["cpu_model"] = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        import numpy
+        blas = numpy.show_config(mode="dicts").get("Build Dependencies", {}).get("blas", {})
+        info["blas"] = f"{blas.get('name')} {blas.get('version')}"
+    except Exception:  # pragma: no cover
+        pass
+    return info
+
+
+def nvml_used_bytes(index: int):
+    """Device memory in use per NVML (None without NVML)."""
+    try:
+        import pynvml
+        pynvml.nvmlInit()
+        try:
+            h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            return int(pynvml.nvmlDeviceGetMemoryInfo(h).used)
+        finally:
+            pynvml.nvmlShutdown()
+    except Exception:
+        return None
+
+
 def oracle_sample_rate(inp_cpu: dict, T: float, sample: int) -> dict:
     """Time the float64 oracle on the first `sample` tokens (tokens/s)."""
     import oracle
@@ -217,7 +251,7 @@ def run_reference(args):
                    "T": cfg.T, "chunk": cfg.chunk,
                    "step": f"oracle over {sample} of the workload's tokens (full V, full W)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last["cores"],
-                         "kind": "oracle",
+                         "kind": "oracle", **host_info(),
                          "sample": f"{sample} tokens of {cfg.name} per step, float64 numpy"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -250,6 +284,10 @@ def run_gpu(args):
 
     torch.cuda.reset_peak_memory_stats(dev)
     mem0 = torch.cuda.memory_allocated(dev)
+    torch.cuda.synchronize(dev)
+    phys_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    nvml0 = nvml_used_bytes(phys_index)
     inp = workloads.make_inputs(cfg, seed=rank, device=dev)
     h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
     gh = torch.empty((N, H), dtype=torch.float32, device=dev)
@@ -272,6 +310,9 @@ def run_gpu(args):
     for _ in range(max(args.warmup, 3) if not args.allow_short_warmup else args.warmup):
         loss = step()
     peak_gib = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
+    nvml1 = nvml_used_bytes(phys_index)
+    # cross-check: device memory NVML sees in use grew by (torch's reserved pool)
+    nvml_delta_gib = (nvml1 - nvml0) / 2**30 if nvml0 is not None and nvml1 is not None else None
 
     gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] \
         if "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
@@ -341,7 +382,7 @@ def run_gpu(args):
         inp_cpu = workloads.make_inputs(cfg, seed=0, n_rows=args.cpu_sample)
         cpu = oracle_sample_rate(inp_cpu, T, args.cpu_sample)
         cpu = {"value": cpu["value"], "unit": "tokens/s", "cores": cpu["cores"],
-               "kind": "oracle",
+               "kind": "oracle", **host_info(),
                "sample": f"first {args.cpu_sample} tokens of {cfg.name} (full V and W), "
                          f"float64 numpy, {cpu['seconds']:.1f} s"}
 
@@ -359,6 +400,7 @@ def run_gpu(args):
         "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
         "frac_bf16_peak_sustained": tflops / peak_sust,
         "peak_gib": peak_gib,
+        "peak_gib_nvml_delta": nvml_delta_gib,
         "loss": loss,
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sust,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
