@@ -281,8 +281,10 @@ def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad
     [N,K], int32 ``found_idx`` [N,K] pre-filled by the caller, float64 ``loss_rows`` [N])
     and the bounded-wait test hook."""
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    # inject_timeout: False / True (= 1, the forward GEMM) or 1..4 (forward,
+    # recompute, grad_hidden, grad_W GEMM of the first chunk)
     opts = _DebugOpts(_ptr(lse) or None, _ptr(zg) or None, _ptr(found_idx) or None,
-                      int(timeout_ns), 1 if inject_timeout else 0, _ptr(loss_rows) or None)
+                      int(timeout_ns), int(inject_timeout), _ptr(loss_rows) or None)
     loss = ctypes.c_float(0.0)
     st = lib().kd_topk_kl_debug(
         _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),

@@ -341,7 +341,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     g.m_tiles = mt; g.n_tiles = p.vt; g.splits = 1;
     g.kb_total = static_cast<int>(cdiv(H, 64));
     g.order = kd::ORDER_M_FAST; g.a_row0 = row0; g.b_row0 = 0;
-    g.timeout_ns = timeout; g.status = dst; g.inject_timeout = (j == 0) ? inject : 0;
+    g.timeout_ns = timeout; g.status = dst; g.inject_timeout = (j == 0 && inject == 1);
     kd::EpiArgs e{};
     e.rows_valid = cj; e.cols_valid = V; e.scale2 = scale2; e.alpha = 1.f;
     e.K = K; e.grow0 = row0; e.c_alloc = p.chunk;
@@ -359,7 +359,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     { ProfScope ps_(PK_LSE, s); KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, mask, lse2,
                                 loss_rows, dbg_lse, dbg_zg, s)); }
 
-    g.inject_timeout = 0;
+    g.inject_timeout = (j == 0 && inject == 2);
     if (store_z) {
       // rows up to the GEMMs' reach get a dZ row (zeros past the chunk)
       const int cover = static_cast<int>(std::min<long long>(p.chunk, cdiv(cj, 256) * 256));
@@ -377,7 +377,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     g2.splits = p.splits;
     g2.kb_total = static_cast<int>(cdiv(V, 64));
     g2.order = kd::ORDER_SPLIT; g2.a_row0 = 0; g2.b_row0 = 0;
-    g2.timeout_ns = timeout; g2.status = dst;
+    g2.timeout_ns = timeout; g2.status = dst; g2.inject_timeout = (j == 0 && inject == 3);
     kd::EpiArgs e2{};
     e2.rows_valid = H; e2.cols_valid = cj; e2.alpha = 1.f; e2.out_row0 = 0;
     e2.split_rows = p.hp;
@@ -394,7 +394,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     g3.splits = 1;
     g3.kb_total = static_cast<int>(cdiv(cj, 64));
     g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = 0;
-    g3.timeout_ns = timeout; g3.status = dst;
+    g3.timeout_ns = timeout; g3.status = dst; g3.inject_timeout = (j == 0 && inject == 4);
     kd::EpiArgs e3{};
     e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
     e3.alpha_dev = alpha_dev;

@@ -211,7 +211,8 @@ kd_status kd_topk_cache_build(const void* hidden, const void* W, int64_t N, int 
  *   loss_rows  double [N] the per-token terms sum_k p (log p - log q_idx),
  *              whose mean is the loss (device)
  *   timeout_ns limit of every device-side wait (0 = the default, 5 s)
- *   inject_timeout  nonzero: the first GEMM's epilogue waits on a barrier
+ *   inject_timeout  1 / 2 / 3 / 4: the first chunk's forward / recompute /
+ *              grad_hidden / grad_W GEMM's epilogue waits on a barrier
  *              that nothing completes, so the call must end with
  *              KD_ERR_TIMEOUT after ~timeout_ns without hanging
  */

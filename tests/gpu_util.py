@@ -32,7 +32,7 @@ def to_device(inp: dict, dev="cuda") -> dict:
     return {k: v.to(dev).contiguous() for k, v in inp.items()}
 
 
-def run_debug(inp: dict, T: float, chunk: int, timeout_ns: int = 0, inject: bool = False):
+def run_debug(inp: dict, T: float, chunk: int, timeout_ns: int = 0, inject: int = 0):
     """Run the CUDA path with every debug export; returns numpy results."""
     h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
     N, H = h.shape

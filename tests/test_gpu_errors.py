@@ -37,11 +37,14 @@ def test_out_of_range_id_is_reported(bad):
     assert ei.value.name == "KD_ERR_INDEX"
 
 
-def test_injected_wait_times_out_and_context_survives():
+@pytest.mark.parametrize("site", [1, 2, 3, 4], ids=["fwd", "recompute", "grad_hidden", "grad_W"])
+def test_injected_wait_times_out_and_context_survives(site):
+    # each GEMM kind (its epilogue, staging and stores) takes the abort and
+    # drain path of a CTA pair once
     inp = _inputs()
     t0 = time.time()
     with pytest.raises(kd.KdError) as ei:
-        run_debug(inp, CFG.T, CFG.chunk, timeout_ns=50_000_000, inject=True)
+        run_debug(inp, CFG.T, CFG.chunk, timeout_ns=50_000_000, inject=site)
     assert ei.value.name == "KD_ERR_TIMEOUT"
     assert time.time() - t0 < 30
     ok = run_debug(inp, CFG.T, CFG.chunk)
