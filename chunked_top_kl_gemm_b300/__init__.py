@@ -132,6 +132,16 @@ def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
+def _on_device(t):
+    """Make t's device current for the library call (it checks pointers and
+    sizes its work against the current device)."""
+    import contextlib
+    import torch
+    if t is None or not t.is_cuda:
+        return contextlib.nullcontext()
+    return torch.cuda.device(t.device)
+
+
 def _stream_handle(stream) -> int:
     import torch
     if stream is None:
@@ -172,9 +182,10 @@ def kd_topk_kl_fwd_bwd(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
     """
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     loss = ctypes.c_float(0.0)
-    st = lib().kd_topk_kl_fwd_bwd(_ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit),
-                                  N, H, V, K, float(T), int(chunk), ctypes.addressof(loss),
-                                  _ptr(grad_hidden), _ptr(grad_W))
+    with _on_device(hidden):
+        st = lib().kd_topk_kl_fwd_bwd(_ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit),
+                                      N, H, V, K, float(T), int(chunk), ctypes.addressof(loss),
+                                      _ptr(grad_hidden), _ptr(grad_W))
     _check(st, "kd_topk_kl_fwd_bwd")
     return float(loss.value)
 
@@ -184,10 +195,11 @@ def kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
     """Caller stream (default: torch's current stream) and workspace tensor."""
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     loss = ctypes.c_float(0.0)
-    st = lib().kd_topk_kl_fwd_bwd_ex(
-        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),
-        int(chunk), ctypes.addressof(loss), _ptr(grad_hidden), _ptr(grad_W),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    with _on_device(hidden):
+        st = lib().kd_topk_kl_fwd_bwd_ex(
+            _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),
+            int(chunk), ctypes.addressof(loss), _ptr(grad_hidden), _ptr(grad_W),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "kd_topk_kl_fwd_bwd_ex")
     return float(loss.value)
 
@@ -212,11 +224,12 @@ def kd_topk_kl_fwd_bwd_masked(hidden, W, topk_idx, topk_logit, token_mask, T: fl
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     token_mask = _check_mask(token_mask, N)
     loss = ctypes.c_float(0.0)
-    st = lib().kd_topk_kl_fwd_bwd_masked(
-        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
-        float(T), int(chunk), 1 if accumulate else 0, ctypes.addressof(loss), _ptr(grad_hidden),
-        _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream_handle(stream))
+    with _on_device(hidden):
+        st = lib().kd_topk_kl_fwd_bwd_masked(
+            _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
+            float(T), int(chunk), 1 if accumulate else 0, ctypes.addressof(loss), _ptr(grad_hidden),
+            _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
     _check(st, "kd_topk_kl_fwd_bwd_masked")
     return float(loss.value)
 
@@ -232,11 +245,12 @@ def kd_topk_kl_fwd_bwd_flags(hidden, W, topk_idx, topk_logit, token_mask, T: flo
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     token_mask = _check_mask(token_mask, N)
     loss = ctypes.c_float(0.0)
-    st = lib().kd_topk_kl_fwd_bwd_flags(
-        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
-        float(T), int(chunk), int(flags), ctypes.addressof(loss), _ptr(grad_hidden),
-        _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream_handle(stream))
+    with _on_device(hidden):
+        st = lib().kd_topk_kl_fwd_bwd_flags(
+            _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
+            float(T), int(chunk), int(flags), ctypes.addressof(loss), _ptr(grad_hidden),
+            _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
     _check(st, "kd_topk_kl_fwd_bwd_flags")
     return float(loss.value)
 
@@ -266,10 +280,11 @@ def kd_topk_cache_build(hidden, W, K: int, chunk: int = 2048, *, topk_idx=None,
         if nbytes == 0:
             raise KdError(1, "kd_topk_cache_workspace_size")
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    st = lib().kd_topk_cache_build(_ptr(hidden), _ptr(W), N, H, V, int(K), int(chunk),
-                                   _ptr(topk_idx), _ptr(topk_logit), _ptr(workspace),
-                                   workspace.numel() * workspace.element_size(),
-                                   _stream_handle(stream))
+    with _on_device(hidden):
+        st = lib().kd_topk_cache_build(_ptr(hidden), _ptr(W), N, H, V, int(K), int(chunk),
+                                       _ptr(topk_idx), _ptr(topk_logit), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream_handle(stream))
     _check(st, "kd_topk_cache_build")
     return topk_idx, topk_logit
 
@@ -286,11 +301,12 @@ def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad
     opts = _DebugOpts(_ptr(lse) or None, _ptr(zg) or None, _ptr(found_idx) or None,
                       int(timeout_ns), int(inject_timeout), _ptr(loss_rows) or None)
     loss = ctypes.c_float(0.0)
-    st = lib().kd_topk_kl_debug(
-        _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),
-        int(chunk), ctypes.addressof(loss), _ptr(grad_hidden), _ptr(grad_W),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream),
-        ctypes.byref(opts))
+    with _on_device(hidden):
+        st = lib().kd_topk_kl_debug(
+            _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), N, H, V, K, float(T),
+            int(chunk), ctypes.addressof(loss), _ptr(grad_hidden), _ptr(grad_W),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream),
+            ctypes.byref(opts))
     _check(st, "kd_topk_kl_debug")
     return float(loss.value)
 
@@ -311,16 +327,22 @@ def kd_gemm_bf16_test(A, B, a_mn: bool, b_mn: bool, bn: int = 0, pair: bool = Fa
     if K2 != K:
         raise ValueError("K mismatch")
     C = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    st = lib().kd_gemm_bf16_test(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(bool(a_mn)),
-                                 int(bool(b_mn)), int(bn), int(pair),
-                                 _stream_handle(stream))
+    with _on_device(A):
+        st = lib().kd_gemm_bf16_test(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(bool(a_mn)),
+                                     int(bool(b_mn)), int(bn), int(pair),
+                                     _stream_handle(stream))
     _check(st, "kd_gemm_bf16_test")
     return C
 
 
 def alloc_workspace(N: int, H: int, V: int, K: int, chunk: int, device=None):
     import torch
-    nbytes = kd_topk_kl_workspace_size(N, H, V, K, chunk)
+    dev = torch.device(device) if device is not None else None
+    if dev is not None and dev.type == "cuda":
+        with torch.cuda.device(dev):
+            nbytes = kd_topk_kl_workspace_size(N, H, V, K, chunk)
+    else:
+        nbytes = kd_topk_kl_workspace_size(N, H, V, K, chunk)
     if nbytes == 0:
         raise KdError(1, "kd_topk_kl_workspace_size")
     # torch allocations are at least 512-byte aligned

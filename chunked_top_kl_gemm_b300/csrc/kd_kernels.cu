@@ -61,22 +61,29 @@ using CfgTestMM2 = GemmCfg<256, true, true, 6, EPI_F32, true>;
 // pair form with two k-blocks per stage (the FWD / DZ ring)
 using CfgTestKK2S = GemmCfg<256, false, false, 3, EPI_F32, true, 2>;
 
-// Work units that can run at once: one per SM, or one per co-resident CTA
-// pair (queried once per instantiation).
+// Work units that can run at once on the current device: one per SM, or one
+// per co-resident CTA pair (queried once per instantiation and device).
 template <class C>
 static int resident_units() {
-  static int cached = 0;
-  if (cached > 0) return cached;
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
   int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if constexpr (!C::CTA2) {
-    cached = sms;
-  } else {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  if (dev >= 0 && dev < kMaxDev && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 148;
+  }
+  int width = sms;
+  if constexpr (C::CTA2) {
+    width = sms / 2;
     if (cudaFuncSetAttribute(kd_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES) != cudaSuccess) {
       cudaGetLastError();
-      return sms / 2;
+      return width;     // no device: do not cache the guess
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -90,26 +97,28 @@ static int resident_units() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kd_gemm_kernel<C>, &cfg) != cudaSuccess ||
-        clusters <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, kd_gemm_kernel<C>, &cfg) == cudaSuccess &&
+        clusters > 0)
+      width = clusters;
+    else
       cudaGetLastError();
-      clusters = sms / 2;
-    }
-    cached = clusters;
   }
-  return cached;
+  if (dev >= 0 && dev < kMaxDev) cached[dev] = width;
+  return width;
 }
 
 template <class C>
 static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                               const GemmArgs& g, const EpiArgs& e, cudaStream_t s) {
-  static bool attr_set = false;  // per instantiation; set once per process
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(kd_gemm_kernel<C>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           C::SMEM_BYTES);
+  static bool attr_set[64] = {};  // per instantiation and device
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    err = cudaFuncSetAttribute(kd_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    attr_set = true;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const long long units = static_cast<long long>(g.m_tiles) * g.n_tiles * g.splits;
   if (units <= 0) return cudaSuccess;
@@ -703,13 +712,15 @@ cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_
                                int c_alloc, int rows_valid, int K, long long row0,
                                int32_t* out_idx, float* out_val, cudaStream_t s) {
   const size_t smem = SEL_CAP * sizeof(unsigned long long) + (SEL_BINS + SEL_THREADS) * 4;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kd_topk_select,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kd_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   kd_topk_select<<<rows_valid, SEL_THREADS, smem, s>>>(z, V, part, n_tiles, c_alloc, K, row0,
                                                        out_idx, out_val);
