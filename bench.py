@@ -466,8 +466,16 @@ def run_sweep(args):
     torch.cuda.set_device(dev)
     kd.lib()
     peaks, _ = load_peaks()
+    oracle_rate = {}   # per workload: the float64 oracle on its first tokens (host cores)
     for name, n_tokens, chunk in SWEEP_POINTS:
         cfg = workloads.CONFIGS[name]
+        if name not in oracle_rate and not args.skip_cpu_baseline:
+            sample = min(cfg.N, args.cpu_sample)
+            r = oracle_sample_rate(workloads.make_inputs(cfg, seed=0, n_rows=sample), cfg.T, sample)
+            oracle_rate[name] = {"value": r["value"], "unit": "tokens/s", "cores": r["cores"],
+                                 "kind": "oracle",
+                                 "sample": f"first {sample} tokens of {name} (full V and W), "
+                                           f"float64 numpy, {r['seconds']:.1f} s"}
         if n_tokens:
             cfg = dataclasses.replace(cfg, N=n_tokens, name=f"{name}_n{n_tokens}")
         chunk = chunk or cfg.chunk
@@ -503,7 +511,8 @@ def run_sweep(args):
             "inputs_gib": sum(workloads.bytes_of_inputs(cfg).values()) / 2**30,
             "grads_gib": 4 * (N * H + V * H) / 2**30,
             "workspace_gib": ws.numel() / 2**30,
-            "dense_fp32_logits_gib": 4 * N * V / 2**30, "loss": loss}), flush=True)
+            "dense_fp32_logits_gib": 4 * N * V / 2**30, "loss": loss,
+            "cpu_baseline": oracle_rate.get(name)}), flush=True)
         del inp, gh, gW, ws, args_
 
 

@@ -23,6 +23,8 @@ LIB_PATH = os.path.join(HERE, "libkdtopk.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "kd_topk_kl.h")
 
 KD_OK = 0
+KD_ERR_INDEX = 3
+KD_ERR_TIMEOUT = 6
 KD_FLAG_ACCUMULATE = 1
 KD_FLAG_STORE_LOGITS = 2
 STATUS_NAMES = {
@@ -74,6 +76,9 @@ def lib() -> ctypes.CDLL:
     L.kd_topk_kl_fwd_bwd_flags.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
                                             ctypes.c_uint, vp, vp, vp, vp, sz, vp]
     L.kd_topk_kl_fwd_bwd_flags.restype = i32
+    L.kd_topk_kl_fwd_bwd_async.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
+                                            ctypes.c_uint, vp, vp, vp, vp, vp, sz, vp]
+    L.kd_topk_kl_fwd_bwd_async.restype = i32
     L.kd_topk_kl_workspace_size_flags.argtypes = [i64, i32, i32, i32, i32, ctypes.c_uint]
     L.kd_topk_kl_workspace_size_flags.restype = sz
     L.kd_topk_cache_workspace_size.argtypes = [i64, i32, i32, i32, i32]
@@ -253,6 +258,34 @@ def kd_topk_kl_fwd_bwd_flags(hidden, W, topk_idx, topk_logit, token_mask, T: flo
             _stream_handle(stream))
     _check(st, "kd_topk_kl_fwd_bwd_flags")
     return float(loss.value)
+
+
+def kd_topk_kl_fwd_bwd_async(hidden, W, topk_idx, topk_logit, token_mask, T: float, chunk: int,
+                             flags: int, loss_out, status_out, grad_hidden, grad_W, workspace,
+                             stream=None) -> None:
+    """Enqueue the call on ``stream`` (default: the current stream) and return
+    at once; capturable in a CUDA graph.  ``loss_out`` (float32 [1]) and
+    ``status_out`` (int32 [1]) are CUDA tensors the last kernel writes; read
+    them after the stream has passed the call (see ``check_status``)."""
+    import torch
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    token_mask = _check_mask(token_mask, N)
+    for name, t, dt in (("loss_out", loss_out, torch.float32), ("status_out", status_out, torch.int32)):
+        if t.dtype != dt or t.numel() < 1 or not t.is_cuda:
+            raise ValueError(f"{name} must be a {dt} CUDA tensor with at least one element")
+    with _on_device(hidden):
+        st = lib().kd_topk_kl_fwd_bwd_async(
+            _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
+            float(T), int(chunk), int(flags), _ptr(loss_out), _ptr(status_out), _ptr(grad_hidden),
+            _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd_async")
+
+
+def check_status(status_out) -> None:
+    """Raise KdError if an asynchronous call's device status word is not KD_OK
+    (reads it: synchronises with the stream that wrote it)."""
+    _check(int(status_out.reshape(-1)[0].item()), "kd_topk_kl_fwd_bwd_async (device status)")
 
 
 def kd_topk_cache_workspace_size(N: int, H: int, V: int, K: int, chunk: int) -> int:

@@ -57,6 +57,9 @@ Profiler& prof() {
   static Profiler p;
   return p;
 }
+// Set while an asynchronous call enqueues: its launches are not timed (the
+// events could only be read after a synchronisation the call does not do).
+thread_local bool t_prof_off = false;
 
 // Bracket one launch.  Returns the index of its event pair or -1.
 struct ProfScope {
@@ -65,7 +68,7 @@ struct ProfScope {
   int slot = -1;
   ProfScope(int kind, cudaStream_t st) {
     Profiler& P = prof();
-    if (!P.on) return;
+    if (!P.on || t_prof_off) return;
     p = &P;
     s = st;
     if (P.ev.size() < 2 * (P.used + 1)) {
@@ -260,16 +263,26 @@ kd_status validate(const void* hidden, const void* W, const int32_t* idx, const 
 // zero gradient rows.  flags: KD_FLAG_ACCUMULATE adds into grad_hidden /
 // grad_W; KD_FLAG_STORE_LOGITS keeps each chunk's fp32 logits from the
 // forward GEMM and forms dZ from them instead of recomputing the GEMM.
+// async (loss_dev and status_dev device words): nothing waits for the
+// stream; the last kernel writes the loss and the status code.
 kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const float* logit,
                    long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
                    float* gW, void* ws, size_t ws_bytes, cudaStream_t s,
-                   const kd_debug_opts* opts, const uint8_t* mask, unsigned flags) {
+                   const kd_debug_opts* opts, const uint8_t* mask, unsigned flags,
+                   float* loss_dev = nullptr, int32_t* status_dev = nullptr) {
+  const bool async = loss_dev != nullptr;
   const int accumulate = (flags & KD_FLAG_ACCUMULATE) ? 1 : 0;
   const bool store_z = (flags & KD_FLAG_STORE_LOGITS) != 0;
   if (flags & ~(KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS)) return KD_ERR_INVALID_ARG;
-  kd_status st = validate(hidden, W, idx, logit, N, H, V, K, T, chunk, loss, gh, gW);
+  kd_status st = validate(hidden, W, idx, logit, N, H, V, K, T, chunk, async ? loss_dev : loss,
+                          gh, gW);
   if (st != KD_OK) return st;
   if (mask && !is_device_ptr(mask)) return KD_ERR_INVALID_ARG;
+  if (async) {
+    if (!status_dev) return KD_ERR_INVALID_ARG;
+    if (!aligned(loss_dev, 4) || !aligned(status_dev, 4)) return KD_ERR_ALIGNMENT;
+    if (!is_device_ptr(loss_dev) || !is_device_ptr(status_dev)) return KD_ERR_INVALID_ARG;
+  }
   const Plan p = make_plan(N, H, V, K, chunk, device_sms(), store_z);
   if (!ws || ws_bytes < p.total) return KD_ERR_OOM;
   prof().used = 0;
@@ -401,11 +414,14 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     e3.first = (j == 0) && !accumulate;
     { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_ht_k, tm_gw, g3, e3, s)); }
   }
-  { ProfScope ps_(PK_FINAL, s); KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, s)); }
+  kd::FinalOut fo{};
+  if (async) fo = kd::FinalOut{loss_dev, status_dev, mask ? 1 : 0, KD_ERR_TIMEOUT, KD_ERR_INDEX};
+  { ProfScope ps_(PK_FINAL, s); KD_CUDA(kd::launch_loss_final(loss_rows, N, dst, fo, s)); }
 
   if (opts && opts->loss_rows)
     KD_CUDA(cudaMemcpyAsync(opts->loss_rows, loss_rows, sizeof(double) * N,
                             cudaMemcpyDeviceToDevice, s));
+  if (async) return KD_OK;
   DevStatus hs{};
   KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
   KD_CUDA(cudaStreamSynchronize(s));
@@ -476,6 +492,28 @@ kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int3
   return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
              workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, token_mask,
              flags);
+}
+
+kd_status kd_topk_kl_fwd_bwd_async(const void* hidden, const void* W, const int32_t* topk_idx,
+                                   const float* topk_logit, const uint8_t* token_mask,
+                                   int64_t N, int H, int V, int K, float T, int chunk,
+                                   unsigned flags, float* loss_dev, int32_t* status_dev,
+                                   float* grad_hidden, float* grad_W, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  t_prof_off = true;
+  const kd_status st = run_impl(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, nullptr,
+                                grad_hidden, grad_W, workspace, workspace_bytes, s, nullptr,
+                                token_mask, flags, loss_dev, status_dev);
+  t_prof_off = false;
+  if (st == KD_ERR_CUDA) {
+    // outside a capture, wait for what was enqueued before the failure
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusActive;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone)
+      cudaStreamSynchronize(s);
+    cudaGetLastError();
+  }
+  return st;
 }
 
 kd_status kd_topk_kl_debug(const void* hidden, const void* W, const int32_t* topk_idx,

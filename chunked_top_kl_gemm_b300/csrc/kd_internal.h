@@ -82,6 +82,14 @@ cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStat
 cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
                                    cudaStream_t s);
 
-cudaError_t launch_loss_final(const double* loss_rows, long long N, DevStatus* st, cudaStream_t s);
+// Device-side results of an asynchronous call (loss == nullptr: none).
+struct FinalOut {
+  float* loss;        // the mean loss over N (masked: over the valid tokens)
+  int* status;        // 0, or code_timeout / code_index from the error word
+  int masked;
+  int code_timeout, code_index;
+};
+cudaError_t launch_loss_final(const double* loss_rows, long long N, DevStatus* st,
+                              const FinalOut& out, cudaStream_t s);
 
 }  // namespace kd

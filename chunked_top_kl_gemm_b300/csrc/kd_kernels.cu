@@ -757,8 +757,11 @@ cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStat
 }
 
 // ------------------------------------------------------------------ final loss
+// Sum of the per-token loss terms into the status block; for an asynchronous
+// call also the mean loss and the status code, into the caller's device words.
 __global__ void __launch_bounds__(1024) kd_loss_final(const double* __restrict__ loss_rows,
-                                                      long long N, DevStatus* st) {
+                                                      long long N, DevStatus* st,
+                                                      const FinalOut out) {
   __shared__ double red[1024];
   double a = 0.0;
   for (long long i = threadIdx.x; i < N; i += 1024) a += loss_rows[i];
@@ -768,11 +771,22 @@ __global__ void __launch_bounds__(1024) kd_loss_final(const double* __restrict__
     if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
     __syncthreads();
   }
-  if (threadIdx.x == 0) st->loss_sum = red[0];
+  if (threadIdx.x == 0) {
+    st->loss_sum = red[0];
+    if (out.loss) {
+      // the mean in double, rounded once to float (as the host does it)
+      const long long n = out.masked ? st->n_valid : N;
+      *out.loss = n > 0 ? static_cast<float>(red[0] / static_cast<double>(n)) : 0.f;
+      const int err = st->err;
+      *out.status = (err & DEV_ERR_TIMEOUT) ? out.code_timeout
+                    : (err & DEV_ERR_INDEX) ? out.code_index : 0;
+    }
+  }
 }
 
-cudaError_t launch_loss_final(const double* loss_rows, long long N, DevStatus* st, cudaStream_t s) {
-  kd_loss_final<<<1, 1024, 0, s>>>(loss_rows, N, st);
+cudaError_t launch_loss_final(const double* loss_rows, long long N, DevStatus* st,
+                              const FinalOut& out, cudaStream_t s) {
+  kd_loss_final<<<1, 1024, 0, s>>>(loss_rows, N, st, out);
   return cudaGetLastError();
 }
 

@@ -175,6 +175,41 @@ kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int3
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Asynchronous form of kd_topk_kl_fwd_bwd_flags, for a training step that
+ * keeps the host out of the loop or captures the step in a CUDA graph.  It
+ * enqueues the whole path on `stream` and returns without synchronising:
+ *
+ *   loss_dev    fp32 [1] (device): the loss, as kd_topk_kl_fwd_bwd_flags
+ *               would return it (the same float, bit for bit)
+ *   status_dev  int32 [1] (device): KD_OK, KD_ERR_INDEX (an id outside
+ *               [0, V)) or KD_ERR_TIMEOUT (a bounded wait ran out), written
+ *               by the call's last kernel
+ *
+ * Both are valid once the stream has reached the end of the call; the
+ * gradients are valid when *status_dev == KD_OK.  The return value covers
+ * only what the host checks before anything is enqueued (arguments,
+ * workspace size, alignment) and CUDA errors while enqueuing; on any return
+ * other than KD_OK nothing of the call needs to be waited for, except after
+ * KD_ERR_CUDA, when the caller synchronises the stream before reusing the
+ * buffers (outside a graph capture the call does so itself).
+ *
+ * Every operation the call enqueues is a kernel launch or a memset on
+ * `stream`, and the TMA descriptors travel by value in the launch
+ * parameters, so the call may be captured into a CUDA graph.  A replay
+ * reuses the pointers and sizes of the capture: new inputs are written into
+ * the same buffers.  The library's per-kernel profiler does not time this
+ * call.  The workspace and both device words belong to the call until the
+ * stream has passed it.  Every other argument as for
+ * kd_topk_kl_fwd_bwd_flags.
+ */
+kd_status kd_topk_kl_fwd_bwd_async(const void* hidden, const void* W, const int32_t* topk_idx,
+                                   const float* topk_logit, const uint8_t* token_mask,
+                                   int64_t N, int H, int V, int K, float T, int chunk,
+                                   unsigned flags, float* loss_dev, int32_t* status_dev,
+                                   float* grad_hidden, float* grad_W, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
  * The offline top-K teacher cache (the step before the loss): per token,
  * the teacher's K highest logits and their ids, computed once and stored
  * (epoka.news, "The two proposed changes"; glonce.com, body;

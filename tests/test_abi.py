@@ -88,3 +88,20 @@ def test_misaligned_tma_pointer_is_alignment_error(L, which):
     ptrs = list(GOOD)
     ptrs[which] += 8
     assert _call(L, ptrs) == 2
+
+
+def _call_async(L, ptrs, loss_dev=0x70000, status_dev=0x80000, N=16, H=64, V=128, K=4):
+    h, w, i, l, gh, gw = ptrs
+    return L.kd_topk_kl_fwd_bwd_async(h, w, i, l, None, N, H, V, K, 1.0, 128, 0, loss_dev,
+                                      status_dev, gh, gw, 0x90000, 1 << 30, None)
+
+
+def test_async_entry_checks_arguments_before_enqueueing(L):
+    assert _call_async(L, GOOD, loss_dev=None) == 1
+    ptrs = list(GOOD)
+    ptrs[0] = None
+    assert _call_async(L, ptrs) == 1
+    ptrs = list(GOOD)
+    ptrs[4] += 8
+    assert _call_async(L, ptrs) == 2
+    assert _call_async(L, GOOD, N=0) == 1
