@@ -610,7 +610,7 @@ namespace {
 
 struct CachePlan {
   int chunk, n_chunks, vt;
-  size_t off_status, off_part, off_z, total;
+  size_t off_status, off_part, off_z, off_tau, off_cnt, off_cand, total;
 };
 
 CachePlan make_cache_plan(long long N, int V, int chunk) {
@@ -626,6 +626,9 @@ CachePlan make_cache_plan(long long N, int V, int chunk) {
   p.off_status = take(sizeof(DevStatus));
   p.off_part = take(sizeof(float2) * p.vt * c);
   p.off_z = take(4ull * c * V);
+  p.off_tau = take(sizeof(float) * c);
+  p.off_cnt = take(sizeof(uint32_t) * c);
+  p.off_cand = take(sizeof(unsigned long long) * c * kd::SEL_GCAP);
   p.total = o;
   return p;
 }
@@ -654,6 +657,9 @@ kd_status cache_build_impl(const void* hidden, const void* W, int64_t N, int H, 
   DevStatus* dst = reinterpret_cast<DevStatus*>(base + p.off_status);
   float2* part = reinterpret_cast<float2*>(base + p.off_part);
   float* zbuf = reinterpret_cast<float*>(base + p.off_z);
+  float* tau = reinterpret_cast<float*>(base + p.off_tau);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(base + p.off_cnt);
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(base + p.off_cand);
 
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tm_hid_k, tm_w_k, tm_z_st;
@@ -683,8 +689,8 @@ kd_status cache_build_impl(const void* hidden, const void* W, int64_t N, int H, 
     { ProfScope ps_(PK_CACHE_GEMM, s);
       KD_CUDA(kd::launch_gemm(kd::GV_FWDZ, tm_hid_k, tm_w_k, tm_z_st, g, e, s)); }
     { ProfScope ps_(PK_CACHE_SELECT, s);
-      KD_CUDA(kd::launch_topk_select(zbuf, V, part, p.vt, p.chunk, cj, K, row0, topk_idx,
-                                     topk_logit, s)); }
+      KD_CUDA(kd::launch_topk_select(zbuf, V, part, p.vt, p.chunk, cj, K, row0, tau, cnt, cand,
+                                     topk_idx, topk_logit, s)); }
   }
   DevStatus hs{};
   KD_CUDA(cudaMemcpyAsync(&hs, dst, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));

@@ -71,10 +71,13 @@ cudaError_t launch_dz_from_z(const float* z, int V, int rows_valid, int rows_cov
 
 // Top-K cache rows [0, rows_valid) of a chunk from its stored logits z
 // [rows][V] and per-tile maxima part[n_tiles][c_alloc].x, written to rows
-// row0.. of out_idx / out_val [N][K].  K <= 8192.
+// row0.. of out_idx / out_val [N][K].  K <= 8192.  Scratch: tau and cnt
+// [rows_valid], cand [rows_valid][SEL_GCAP].
+constexpr int SEL_GCAP = 2048;   // candidates one row's list holds
 cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_tiles,
-                               int c_alloc, int rows_valid, int K, long long row0,
-                               int32_t* out_idx, float* out_val, cudaStream_t s);
+                               int c_alloc, int rows_valid, int K, long long row0, float* tau,
+                               uint32_t* cnt, unsigned long long* cand, int32_t* out_idx,
+                               float* out_val, cudaStream_t s);
 
 cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStatus* st,
                               cudaStream_t s);

@@ -530,16 +530,32 @@ cudaError_t launch_dz_from_z(const float* z, int V, int rows_valid, int rows_cov
 // a candidate is the 64-bit (key << 32 | ~id), so sorting candidates in
 // decreasing order sorts by value, then by increasing id.
 //
-// Fast path: the K-th largest of the row's per-tile maxima (from the GEMM
-// epilogue) is a lower bound of its K-th largest value, since K tiles hold a
-// value at least that large; one pass collects every value at or above it
-// (typically about K of them) and a bitonic sort orders them.  Exact path,
-// when the candidates overflow shared memory (or K exceeds the tile count):
-// a three-pass radix select finds the K-th largest key, then the larger keys
-// and, in increasing id order, enough of the equal keys are gathered.
-constexpr int SEL_THREADS = 512;
-constexpr int SEL_CAP = 8192;          // candidates a block holds (>= K)
+// Four stream-ordered kernels per chunk:
+//   kd_sel_tau     the K-th largest of the row's per-tile maxima (from the
+//                  GEMM epilogue): a lower bound tau0 of the row's K-th
+//                  largest value, since K tiles hold a value at least that
+//                  large (-inf when K exceeds the tile count);
+//   kd_sel_filter  one streaming pass over the whole chunk: every value
+//                  >= tau0 is appended to its row's candidate list
+//                  (typically about K of them; warp-aggregated counters);
+//   kd_sel_sort    rows with at most SEL_GCAP candidates: bitonic sort of
+//                  the list, the first K written out;
+//   kd_sel_exact   every other row (its list overflowed; fewer than K
+//                  candidates cannot happen, but would land here too): a three-pass radix select
+//                  finds the K-th largest key, then the larger keys and, in
+//                  increasing id order, enough of the equal keys are
+//                  gathered and sorted.
+// The filter is the only pass over the logits on the fast path, so it runs
+// as a flat, evenly loaded stream at HBM speed; the per-row work (threshold,
+// sort) is tiny and runs in kernels of its own.
+constexpr int SEL_THREADS = 512;       // exact path
+constexpr int SEL_CAP = 8192;          // exact path: keys a block holds (>= K)
 constexpr int SEL_BINS = 2048;
+constexpr int SEL_TAU_THREADS = 128;   // one row per warp
+constexpr int SEL_TAU_MAX = 2048;      // tile maxima a warp holds (vocabularies <= 524,288)
+constexpr int FLT_THREADS = 256;
+constexpr int FLT_UNROLL = 8;          // 16-byte loads in flight per thread
+constexpr int SORT_THREADS = 256;
 
 __device__ __forceinline__ uint32_t sel_key(float f) {
   const uint32_t b = __float_as_uint(f + 0.0f);      // -0 -> +0
@@ -551,12 +567,17 @@ __device__ __forceinline__ float sel_val(uint32_t k) {
 __device__ __forceinline__ unsigned long long sel_cand(uint32_t key, int id) {
   return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~id);
 }
+__device__ __forceinline__ int sel_pow2(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
 
 // Sort s[0..P) (P a power of two) in decreasing order; all threads call.
 __device__ void sel_bitonic_desc(unsigned long long* s, int P) {
   for (int k = 2; k <= P; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < P; i += SEL_THREADS) {
+      for (int i = threadIdx.x; i < P; i += blockDim.x) {
         const int ixj = i ^ j;
         if (ixj > i) {
           const unsigned long long a = s[i], b = s[ixj];
@@ -569,161 +590,221 @@ __device__ void sel_bitonic_desc(unsigned long long* s, int P) {
   }
 }
 
-__global__ void __launch_bounds__(SEL_THREADS) kd_topk_select(
-    const float* __restrict__ z, int V, const float2* __restrict__ part, int n_tiles,
-    int c_alloc, int K, long long row0, int32_t* __restrict__ out_idx, float* __restrict__ out_val) {
-  extern __shared__ unsigned long long cand[];                    // [SEL_CAP]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(cand + SEL_CAP);    // [SEL_BINS]
-  uint32_t* scan = hist + SEL_BINS;                                 // [SEL_THREADS]
-  __shared__ uint32_t s_cnt, s_prefix, s_rank;
-  const int r = blockIdx.x, tid = threadIdx.x;
-  const float* zr = z + static_cast<long long>(r) * V;
-  auto pow2 = [](int n) { int p = 1; while (p < n) p <<= 1; return p; };
-
-  // 1) lower bound of the K-th largest value: the K-th largest tile maximum.
-  // Tile maximum i is the K-th largest when exactly K - 1 others precede it
-  // in (value descending, index ascending) order.
-  __shared__ float s_tau0;
-  if (tid == 0) s_tau0 = -CUDART_INF_F;
-  float* tmax = reinterpret_cast<float*>(cand);
-  if (K <= n_tiles && n_tiles <= 2 * SEL_CAP) {
-    for (int t = tid; t < n_tiles; t += SEL_THREADS)
-      tmax[t] = part[static_cast<long long>(t) * c_alloc + r].x + 0.0f;
-    __syncthreads();
-    for (int i = tid; i < n_tiles; i += SEL_THREADS) {
-      const float mi = tmax[i];
-      int before = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const float mj = tmax[j];
-        before += (mj > mi) || (mj == mi && j < i);
-      }
-      if (before == K - 1) s_tau0 = mi;
-    }
-  }
-  if (tid == 0) s_cnt = 0;
-  __syncthreads();
-  const float tau0 = s_tau0;
-
-  // 2) every value >= tau0 (at least K of them); four 16-byte streaming
-  // loads in flight per thread
-  auto take = [&](float x, int id) {
-    if (x >= tau0) {
-      const uint32_t slot = atomicAdd(&s_cnt, 1u);
-      if (slot < SEL_CAP) cand[slot] = sel_cand(sel_key(x), id);
-    }
-  };
-  const float4* z4 = reinterpret_cast<const float4*>(zr);
-  const int V4 = V >> 2;
-  int i4 = tid;
-  for (; i4 + 3 * SEL_THREADS < V4; i4 += 4 * SEL_THREADS) {
-    float4 x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = __ldcs(z4 + i4 + u * SEL_THREADS);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = (i4 + u * SEL_THREADS) * 4;
-      take(x[u].x, v); take(x[u].y, v + 1); take(x[u].z, v + 2); take(x[u].w, v + 3);
-    }
-  }
-  for (; i4 < V4; i4 += SEL_THREADS) {
-    const float4 x = __ldcs(z4 + i4);
-    const int v = i4 * 4;
-    take(x.x, v); take(x.y, v + 1); take(x.z, v + 2); take(x.w, v + 3);
-  }
-  __syncthreads();
-  int n = static_cast<int>(s_cnt);
-
-  if (n > SEL_CAP) {
-    // 3) exact K-th largest key by radix select (11 + 11 + 10 bits)
-    uint32_t prefix = 0, pmask = 0, kk = static_cast<uint32_t>(K);
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int sh = shifts[pass], nb = 1 << widths[pass];
-      for (int b = tid; b < nb; b += SEL_THREADS) hist[b] = 0;
-      __syncthreads();
-      for (int v = tid; v < V; v += SEL_THREADS) {
-        const uint32_t key = sel_key(zr[v]);
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
-      }
-      __syncthreads();
-      if (tid == 0) {
-        uint32_t above = 0;
-        int b = nb - 1;
-        for (; b > 0; --b) {
-          if (above + hist[b] >= kk) break;
-          above += hist[b];
-        }
-        s_prefix = prefix | (static_cast<uint32_t>(b) << sh);
-        s_rank = kk - above;
-      }
-      __syncthreads();
-      prefix = s_prefix;
-      kk = s_rank;
-      pmask |= static_cast<uint32_t>(nb - 1) << sh;
-      __syncthreads();
-    }
-    const uint32_t tau = prefix;                   // the K-th largest key
-    const int need = static_cast<int>(kk);         // equal keys to take
-    // 4) the keys above tau (fewer than K)
-    if (tid == 0) s_cnt = 0;
-    __syncthreads();
-    for (int v = tid; v < V; v += SEL_THREADS) {
-      const uint32_t key = sel_key(zr[v]);
-      if (key > tau) cand[atomicAdd(&s_cnt, 1u)] = sel_cand(key, v);
-    }
-    __syncthreads();
-    const int n_gt = static_cast<int>(s_cnt);
-    // 5) the `need` lowest ids among the keys equal to tau: each thread scans
-    // a contiguous id range; an exclusive scan of the counts orders them
-    const int L = (V + SEL_THREADS - 1) / SEL_THREADS;
-    const int v0 = tid * L, v1 = min(V, v0 + L);
-    uint32_t mine = 0;
-    for (int v = v0; v < v1; ++v) mine += sel_key(zr[v]) == tau;
-    scan[tid] = mine;
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t acc = 0;
-      for (int i = 0; i < SEL_THREADS; ++i) { const uint32_t c = scan[i]; scan[i] = acc; acc += c; }
-    }
-    __syncthreads();
-    uint32_t rank = scan[tid];
-    for (int v = v0; v < v1 && rank < static_cast<uint32_t>(need); ++v) {
-      if (sel_key(zr[v]) == tau) { cand[n_gt + rank] = sel_cand(tau, v); ++rank; }
-    }
-    __syncthreads();
-    n = K;
-  }
-
-  // 6) order the candidates and write the first K
-  const int P = pow2(n);
-  for (int i = n + tid; i < P; i += SEL_THREADS) cand[i] = 0ull;
-  __syncthreads();
-  sel_bitonic_desc(cand, P);
-  const long long o = (row0 + r) * static_cast<long long>(K);
-  for (int k = tid; k < K; k += SEL_THREADS) {
-    const unsigned long long c = cand[k];
+// Write the first K sorted candidates of a row.
+__device__ __forceinline__ void sel_write(const unsigned long long* s, int K, long long row,
+                                          int32_t* out_idx, float* out_val) {
+  const long long o = row * static_cast<long long>(K);
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const unsigned long long c = s[k];
     out_val[o + k] = sel_val(static_cast<uint32_t>(c >> 32));
     out_idx[o + k] = static_cast<int32_t>(~static_cast<uint32_t>(c));
   }
 }
 
+// tau0 of one row per warp, and the row's candidate count reset.  The K-th
+// largest of the row's n_tiles tile-maximum keys, found bit by bit from the
+// top: the largest key t with at least K keys >= t.
+__global__ void __launch_bounds__(SEL_TAU_THREADS) kd_sel_tau(const float2* __restrict__ part,
+                                                              int n_tiles, int c_alloc,
+                                                              int rows_valid, int K,
+                                                              float* __restrict__ tau,
+                                                              uint32_t* __restrict__ cnt) {
+  __shared__ uint32_t keys[SEL_TAU_THREADS / 32][SEL_TAU_MAX];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (SEL_TAU_THREADS / 32) + warp;
+  if (r >= rows_valid) return;                       // warp-uniform
+  float t0 = -CUDART_INF_F;
+  if (K <= n_tiles && n_tiles <= SEL_TAU_MAX) {
+    uint32_t* k = keys[warp];
+    for (int t = lane; t < n_tiles; t += 32)
+      k[t] = sel_key(part[static_cast<long long>(t) * c_alloc + r].x);
+    __syncwarp();
+    uint32_t prefix = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t c = prefix | (1u << bit);
+      uint32_t n = 0;
+      for (int t = lane; t < n_tiles; t += 32) n += k[t] >= c;
+      if (__reduce_add_sync(0xffffffffu, n) >= static_cast<uint32_t>(K)) prefix = c;
+    }
+    t0 = sel_val(prefix);
+  }
+  if (lane == 0) {
+    tau[r] = t0;
+    cnt[r] = 0;
+  }
+}
+
+// Values >= tau0 of row blockIdx.y, columns of this block's segment of
+// FLT_THREADS x FLT_UNROLL float4s.  A list holds SEL_GCAP candidates; the
+// count goes on past it, so a count above SEL_GCAP marks an overflow.
+__global__ void __launch_bounds__(FLT_THREADS) kd_sel_filter(const float* __restrict__ z, int V,
+                                                             const float* __restrict__ tau,
+                                                             uint32_t* __restrict__ cnt,
+                                                             unsigned long long* __restrict__ cand) {
+  const int r = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const float t0 = __ldg(tau + r);
+  const float4* z4 = reinterpret_cast<const float4*>(z + static_cast<long long>(r) * V);
+  const int V4 = V >> 2;                      // V is a multiple of 8
+  const int i0 = blockIdx.x * (FLT_THREADS * FLT_UNROLL) + threadIdx.x;
+  float4 x[FLT_UNROLL];
+#pragma unroll
+  for (int u = 0; u < FLT_UNROLL; ++u) {
+    const int i = i0 + u * FLT_THREADS;
+    x[u] = i < V4 ? __ldcs(z4 + i) : make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F,
+                                                 -CUDART_INF_F);
+  }
+  unsigned long long* list = cand + static_cast<long long>(r) * SEL_GCAP;
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int u = 0; u < FLT_UNROLL; ++u) {
+    const int i = i0 + u * FLT_THREADS;
+    const float v4[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const bool pass = i < V4 && v4[c] >= t0;
+      const unsigned m = __ballot_sync(0xffffffffu, pass);
+      if (m == 0u) continue;                  // warp-uniform
+      uint32_t base = 0;
+      const int leader = __ffs(m) - 1;
+      if (lane == leader) base = atomicAdd(cnt + r, static_cast<uint32_t>(__popc(m)));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      if (pass) {
+        const uint32_t slot = base + __popc(m & lt);
+        if (slot < SEL_GCAP) list[slot] = sel_cand(sel_key(v4[c]), 4 * i + c);
+      }
+    }
+  }
+}
+
+// Rows whose list did not overflow: sort it and write the first K.
+__global__ void __launch_bounds__(SORT_THREADS) kd_sel_sort(const uint32_t* __restrict__ cnt,
+                                                            const unsigned long long* __restrict__ cand,
+                                                            int K, long long row0,
+                                                            int32_t* __restrict__ out_idx,
+                                                            float* __restrict__ out_val) {
+  __shared__ unsigned long long s[SEL_GCAP];
+  const int r = blockIdx.x;
+  const int n = static_cast<int>(cnt[r]);
+  if (n > SEL_GCAP || n < K) return;          // kd_sel_exact takes this row
+  const int P = sel_pow2(n);
+  const unsigned long long* list = cand + static_cast<long long>(r) * SEL_GCAP;
+  for (int i = threadIdx.x; i < P; i += SORT_THREADS) s[i] = i < n ? list[i] : 0ull;
+  __syncthreads();
+  sel_bitonic_desc(s, P);
+  sel_write(s, K, row0 + r, out_idx, out_val);
+}
+
+// Rows whose list overflowed: exact K-th largest key by radix select
+// (11 + 11 + 10 bits), then the keys above it and the lowest ids among the
+// keys equal to it.
+__global__ void __launch_bounds__(SEL_THREADS) kd_sel_exact(const float* __restrict__ z, int V,
+                                                            const uint32_t* __restrict__ cnt,
+                                                            int K, long long row0,
+                                                            int32_t* __restrict__ out_idx,
+                                                            float* __restrict__ out_val) {
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const uint32_t n = cnt[r];
+  if (n <= static_cast<uint32_t>(SEL_GCAP) && n >= static_cast<uint32_t>(K)) return;   // sorted
+  extern __shared__ unsigned long long kcand[];                     // [SEL_CAP]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(kcand + SEL_CAP);    // [SEL_BINS]
+  uint32_t* scan = hist + SEL_BINS;                                  // [SEL_THREADS]
+  __shared__ uint32_t s_cnt, s_prefix, s_rank;
+  const float* zr = z + static_cast<long long>(r) * V;
+
+  uint32_t prefix = 0, pmask = 0, kk = static_cast<uint32_t>(K);
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = shifts[pass], nb = 1 << widths[pass];
+    for (int b = tid; b < nb; b += SEL_THREADS) hist[b] = 0;
+    __syncthreads();
+    for (int v = tid; v < V; v += SEL_THREADS) {
+      const uint32_t key = sel_key(zr[v]);
+      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t above = 0;
+      int b = nb - 1;
+      for (; b > 0; --b) {
+        if (above + hist[b] >= kk) break;
+        above += hist[b];
+      }
+      s_prefix = prefix | (static_cast<uint32_t>(b) << sh);
+      s_rank = kk - above;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    kk = s_rank;
+    pmask |= static_cast<uint32_t>(nb - 1) << sh;
+    __syncthreads();
+  }
+  const uint32_t tau = prefix;                   // the K-th largest key
+  const int need = static_cast<int>(kk);         // equal keys to take
+  // the keys above tau (fewer than K)
+  if (tid == 0) s_cnt = 0;
+  __syncthreads();
+  for (int v = tid; v < V; v += SEL_THREADS) {
+    const uint32_t key = sel_key(zr[v]);
+    if (key > tau) kcand[atomicAdd(&s_cnt, 1u)] = sel_cand(key, v);
+  }
+  __syncthreads();
+  const int n_gt = static_cast<int>(s_cnt);
+  // the `need` lowest ids among the keys equal to tau: each thread scans a
+  // contiguous id range; an exclusive scan of the counts orders them
+  const int L = (V + SEL_THREADS - 1) / SEL_THREADS;
+  const int v0 = tid * L, v1 = min(V, v0 + L);
+  uint32_t mine = 0;
+  for (int v = v0; v < v1; ++v) mine += sel_key(zr[v]) == tau;
+  scan[tid] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t acc = 0;
+    for (int i = 0; i < SEL_THREADS; ++i) { const uint32_t c = scan[i]; scan[i] = acc; acc += c; }
+  }
+  __syncthreads();
+  uint32_t rank = scan[tid];
+  for (int v = v0; v < v1 && rank < static_cast<uint32_t>(need); ++v) {
+    if (sel_key(zr[v]) == tau) { kcand[n_gt + rank] = sel_cand(tau, v); ++rank; }
+  }
+  __syncthreads();
+  const int P = sel_pow2(K);
+  for (int i = K + tid; i < P; i += SEL_THREADS) kcand[i] = 0ull;
+  __syncthreads();
+  sel_bitonic_desc(kcand, P);
+  sel_write(kcand, K, row0 + r, out_idx, out_val);
+}
+
 cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_tiles,
-                               int c_alloc, int rows_valid, int K, long long row0,
-                               int32_t* out_idx, float* out_val, cudaStream_t s) {
+                               int c_alloc, int rows_valid, int K, long long row0, float* tau,
+                               uint32_t* cnt, unsigned long long* cand, int32_t* out_idx,
+                               float* out_val, cudaStream_t s) {
   const size_t smem = SEL_CAP * sizeof(unsigned long long) + (SEL_BINS + SEL_THREADS) * 4;
   static bool attr_set[64] = {};  // per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kd_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(kd_sel_exact, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kd_topk_select<<<rows_valid, SEL_THREADS, smem, s>>>(z, V, part, n_tiles, c_alloc, K, row0,
-                                                       out_idx, out_val);
+  constexpr int rows_per_block = SEL_TAU_THREADS / 32;
+  kd_sel_tau<<<(rows_valid + rows_per_block - 1) / rows_per_block, SEL_TAU_THREADS, 0, s>>>(
+      part, n_tiles, c_alloc, rows_valid, K, tau, cnt);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int V4 = V / 4;
+  dim3 fgrid((V4 + FLT_THREADS * FLT_UNROLL - 1) / (FLT_THREADS * FLT_UNROLL), rows_valid);
+  kd_sel_filter<<<fgrid, FLT_THREADS, 0, s>>>(z, V, tau, cnt, cand);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kd_sel_sort<<<rows_valid, SORT_THREADS, 0, s>>>(cnt, cand, K, row0, out_idx, out_val);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kd_sel_exact<<<rows_valid, SEL_THREADS, smem, s>>>(z, V, cnt, K, row0, out_idx, out_val);
   return cudaGetLastError();
 }
 
