@@ -553,7 +553,7 @@ constexpr int SEL_CAP = 8192;          // exact path: keys a block holds (>= K)
 constexpr int SEL_BINS = 2048;
 constexpr int SEL_TAU_THREADS = 128;   // one row per warp
 constexpr int SEL_TAU_MAX = 2048;      // tile maxima a warp holds (vocabularies <= 524,288)
-constexpr int FLT_THREADS = 256;
+constexpr int FLT_THREADS = 128;
 constexpr int FLT_UNROLL = 8;          // 16-byte loads in flight per thread
 constexpr int SORT_THREADS = 256;
 
@@ -616,8 +616,9 @@ __global__ void __launch_bounds__(SEL_TAU_THREADS) kd_sel_tau(const float2* __re
   float t0 = -CUDART_INF_F;
   if (K <= n_tiles && n_tiles <= SEL_TAU_MAX) {
     uint32_t* k = keys[warp];
-    for (int t = lane; t < n_tiles; t += 32)
-      k[t] = sel_key(part[static_cast<long long>(t) * c_alloc + r].x);
+#pragma unroll 8
+    for (int t = lane; t < n_tiles; t += 32)   // strided L2 reads: keep several in flight
+      k[t] = sel_key(__ldg(&part[static_cast<long long>(t) * c_alloc + r].x));
     __syncwarp();
     uint32_t prefix = 0;
     for (int bit = 31; bit >= 0; --bit) {
