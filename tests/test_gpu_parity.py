@@ -48,13 +48,18 @@ CASES = {
 
 # Degenerate and extreme sizes: H below one 64-deep k-block, a vocabulary
 # below one 256-wide tile (the pair multiplies 32 columns), teacher ids that
-# cover half the vocabulary (about 128 hits per row and vocab tile), and the
-# largest K the library accepts.
+# cover half the vocabulary (about 128 hits per row and vocab tile), the
+# largest K the library accepts, and extreme temperatures.
 EDGE = {
     "h8_v8": workloads.custom("h8v8", N=33, H=8, V=8, K=3, T=1.0, chunk=128),
     "h24_v40_k_eq_v": workloads.custom("h24", N=200, H=24, V=40, K=40, T=0.5, chunk=64),
     "dense_hits": workloads.custom("dense", N=130, H=64, V=4096, K=2048, T=1.0, chunk=128),
     "k_max": workloads.custom("kmax", N=64, H=72, V=16384, K=8192, T=1.3, chunk=64),
+    # temperature extremes: a sharp student softmax (z/T spans ~20) and a
+    # nearly uniform one
+    "cold_T0.1": workloads.custom("cold", N=300, H=256, V=4096, K=32, T=0.1, chunk=128,
+                                  hidden_rms_norm=True, teacher="zipf"),
+    "hot_T20": workloads.custom("hot", N=300, H=256, V=4096, K=32, T=20.0, chunk=128),
 }
 CASES.update(EDGE)
 
