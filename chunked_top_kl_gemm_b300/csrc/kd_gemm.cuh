@@ -30,7 +30,8 @@
 //              logits kept for a backward pass without recompute).
 //   EPI_F32  : alpha * D stored as fp32 through TMA.
 //   EPI_ACC  : alpha * D added into an fp32 tensor by TMA reduce-add
-//              (plain store when `first`).
+//              (plain store when `first`), paced over the next unit's main
+//              loop (see the epilogue).
 #pragma once
 #include "kd_args.h"
 #include "kd_ptx.cuh"
@@ -71,6 +72,7 @@ struct GemmCfg {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(!B_MN || BN_CTA % 64 == 0, "MN-major B boxes are 64 wide");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert((2 * STAGES + 6) * 8 + 4 * 4 <= BAR_BYTES, "barrier area");
 };
 
 struct Unit {
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(inj_bar + 1);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  volatile uint32_t* prod_progress = reinterpret_cast<volatile uint32_t*>(tmem_slot + 3);  // EPI_ACC
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(inj_bar, 1);
     *abort_word = 0;
     *peer_issued = 0;
+    *prod_progress = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           ++issued;
+          if constexpr (C::KIND == EPI_ACC) *prod_progress = issued;   // read by the pacing
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -367,8 +372,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = mbar_wait(inj_bar, 0, w, SITE_INJECT);
     }
     int lt = 0;
+    uint32_t stages_done = 0;   // EPI_ACC: ring stages of the units up to this one
     for (int u = unit0; u < units && ok; u += ustep, ++lt) {
       const Unit t = unit_of(u, g);
+      // EPI_ACC pacing: the stages the producer will have issued when this
+      // unit's loads end, and the stage count of the unit after it (0: none)
+      uint32_t next_stages = 0;
+      if constexpr (C::KIND == EPI_ACC) {
+        stages_done += static_cast<uint32_t>((t.kb1 - t.kb0 + C::KSUB - 1) / C::KSUB);
+        if (u + ustep < units) {
+          const Unit tn = unit_of(u + ustep, g);
+          next_stages = static_cast<uint32_t>((tn.kb1 - tn.kb0 + C::KSUB - 1) / C::KSUB);
+        }
+      }
       const int acc = lt & 1;
       const uint32_t acc_par = (lt >> 1) & 1;
       const int slab0 = t.m * C::TILE_M + static_cast<int>(rank) * BM;   // first row of the slab
@@ -508,6 +524,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int sb = 0; sb < C::BN / 32; ++sb) {
           const int c0 = sb * 32;
           if (!box_ok || t.n * C::BN + c0 >= e.cols_valid) break;   // warp-uniform
+          if constexpr (C::KIND == EPI_ACC) {
+            // 128 KB of reduce-adds per CTA issued at once delay the next
+            // unit's operand loads (same TMA unit, same L2 slices): box sb
+            // waits until the producer has issued sb / 8 of the first three
+            // quarters of the next unit's stages.  Bounded; the last unit
+            // of a CTA (no next unit) is not paced.
+            if (sb > 0 && next_stages > 0) {
+              const uint32_t target =
+                  stages_done + (3u * static_cast<uint32_t>(sb) * next_stages) / (4u * (C::BN / 32));
+              for (int it = 0; it < 512 && *prod_progress < target && !*abort_word; ++it)
+                __nanosleep(64);
+            }
+          }
           uint32_t r[32];
           tmem_ld32(tb + c0, r);
           tmem_ld_wait();
