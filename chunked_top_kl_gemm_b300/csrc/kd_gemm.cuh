@@ -30,8 +30,9 @@
 //              logits kept for a backward pass without recompute).
 //   EPI_F32  : alpha * D stored as fp32 through TMA.
 //   EPI_ACC  : alpha * D added into an fp32 tensor by TMA reduce-add
-//              (plain store when `first`), paced over the next unit's main
-//              loop (see the epilogue).
+//              (plain store when `first`).
+// EPI_FWDZ and EPI_ACC pace their TMA writes over the next unit's operand
+// loads (see the epilogue).
 #pragma once
 #include "kd_args.h"
 #include "kd_ptx.cuh"
@@ -66,6 +67,11 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TX_BYTES = NCTA * STAGE_BYTES;   // one stage of the whole pair
   static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  // epilogues that write 128 KB of fp32 per CTA and tile pace those writes
+  // over the next tile's operand loads (see the epilogue); DZ's 64 KB of
+  // bf16 ran slower paced and is written at once
+  static constexpr bool PACED = KIND == EPI_ACC || KIND == EPI_FWDZ;
+  static constexpr int OUT_BOXES = BN / 32;   // fp32 32-column boxes per warp and tile
   static constexpr int EPI_BYTES = (KIND == EPI_FWD) ? 0 : 4 * 2 * EPI_STAGE_BYTES;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(inj_bar + 1);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
-  volatile uint32_t* prod_progress = reinterpret_cast<volatile uint32_t*>(tmem_slot + 3);  // EPI_ACC
+  volatile uint32_t* prod_progress = reinterpret_cast<volatile uint32_t*>(tmem_slot + 3);  // PACED
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -274,7 +280,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           ++issued;
-          if constexpr (C::KIND == EPI_ACC) *prod_progress = issued;   // read by the pacing
+          if constexpr (C::PACED) *prod_progress = issued;   // read by the epilogue's pacing
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -371,14 +377,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (g.inject_timeout) {
       ok = mbar_wait(inj_bar, 0, w, SITE_INJECT);
     }
+    // Output pacing.  A tile's TMA writes issued as one burst (128 KB per
+    // CTA) delay the next tile's operand loads, which share the TMA unit and
+    // the L2 with them.  Box sb of a tile's OUT_BOXES therefore waits until
+    // the producer has issued sb / OUT_BOXES of the first three quarters of
+    // the next tile's ring stages.  The wait is bounded and gives up on
+    // abort; the last tile of a CTA (no next tile) is not paced.
+    uint32_t stages_done = 0;   // ring stages of the units up to this one
+    uint32_t next_stages = 0;   // ring stages of the next unit (0: none)
+    auto pace = [&](int sb) {
+      if (sb > 0 && next_stages > 0) {
+        const uint32_t target = stages_done + (3u * static_cast<uint32_t>(sb) * next_stages) /
+                                                  (4u * static_cast<uint32_t>(C::OUT_BOXES));
+        for (int it = 0; it < 512 && *prod_progress < target && !*abort_word; ++it)
+          __nanosleep(64);
+      }
+    };
     int lt = 0;
-    uint32_t stages_done = 0;   // EPI_ACC: ring stages of the units up to this one
     for (int u = unit0; u < units && ok; u += ustep, ++lt) {
       const Unit t = unit_of(u, g);
-      // EPI_ACC pacing: the stages the producer will have issued when this
-      // unit's loads end, and the stage count of the unit after it (0: none)
-      uint32_t next_stages = 0;
-      if constexpr (C::KIND == EPI_ACC) {
+      if constexpr (C::PACED) {
+        next_stages = 0;
         stages_done += static_cast<uint32_t>((t.kb1 - t.kb0 + C::KSUB - 1) / C::KSUB);
         if (u + ustep < units) {
           const Unit tn = unit_of(u + ustep, g);
@@ -446,6 +465,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (nvalid <= 0) continue;
           if constexpr (C::KIND == EPI_FWDZ) {
             if (box_row0 < e.c_alloc) {                  // warp-uniform: inside the z tensor
+              pace(b);
               const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
               if (lane == 0) bulk_wait_read<1>();
               __syncwarp();
@@ -524,19 +544,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int sb = 0; sb < C::BN / 32; ++sb) {
           const int c0 = sb * 32;
           if (!box_ok || t.n * C::BN + c0 >= e.cols_valid) break;   // warp-uniform
-          if constexpr (C::KIND == EPI_ACC) {
-            // 128 KB of reduce-adds per CTA issued at once delay the next
-            // unit's operand loads (same TMA unit, same L2 slices): box sb
-            // waits until the producer has issued sb / 8 of the first three
-            // quarters of the next unit's stages.  Bounded; the last unit
-            // of a CTA (no next unit) is not paced.
-            if (sb > 0 && next_stages > 0) {
-              const uint32_t target =
-                  stages_done + (3u * static_cast<uint32_t>(sb) * next_stages) / (4u * (C::BN / 32));
-              for (int it = 0; it < 512 && *prod_progress < target && !*abort_word; ++it)
-                __nanosleep(64);
-            }
-          }
+          pace(sb);
           uint32_t r[32];
           tmem_ld32(tb + c0, r);
           tmem_ld_wait();
