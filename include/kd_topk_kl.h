@@ -220,6 +220,7 @@ kd_status kd_topk_kl_fwd_bwd_async(const void* hidden, const void* W, const int3
  *   K           1 <= K <= min(V, 8192)
  *   chunk       token rows per chunk (rounded up to a multiple of 128); the
  *               workspace holds one chunk's fp32 logits (chunk x V x 4 bytes)
+ *               and a 16 KB candidate list per row of the chunk
  *   topk_idx    int32 [N, K] out (device): ids in decreasing logit order,
  *               equal logits in increasing id order (the pages leave ties open)
  *   topk_logit  fp32 [N, K] out (device): the logits z (fp32 accumulation of
