@@ -42,10 +42,12 @@
  * Errors.  Argument errors are detected on the host before anything is
  * launched.  Device-side errors (an id outside [0, V), a bounded wait that
  * ran out) are reported after the stream has been synchronised; on any
- * error the outputs are unspecified.  Every call returns after a stream
- * synchronisation (also after a CUDA error part-way through), because
- * `loss` is a host pointer: when it returns, none of its kernels still uses
- * the workspace or the outputs.
+ * error the outputs are unspecified.  Every call except
+ * kd_topk_kl_fwd_bwd_async returns after a stream synchronisation (also
+ * after a CUDA error part-way through), because `loss` is a host pointer:
+ * when it returns, none of its kernels still uses the workspace or the
+ * outputs.  kd_topk_kl_fwd_bwd_async leaves the loss and the device-side
+ * status in device memory and does not wait (see there).
  *
  * Thread safety.  Calls on different streams may run concurrently if they
  * use different workspaces.
