@@ -195,18 +195,38 @@ def host_info() -> dict:
     return info
 
 
-def nvml_used_bytes(index: int):
-    """Device memory in use per NVML (None without NVML)."""
+def nvml_used_bytes(dev):
+    """Device memory in use per NVML on the GPU behind torch device `dev`, in
+    bytes (None when it cannot be read).  Through pynvml when it is
+    installed, else through nvidia-smi (NVML's command-line front end, MiB
+    resolution).  The device is matched by its UUID: NVML's numbering need
+    not follow CUDA_VISIBLE_DEVICES."""
+    import torch
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if uuid is None:
+        return None
     try:
         import pynvml
-        pynvml.nvmlInit()
+    except ImportError:
+        pynvml = None
+    if pynvml is not None:
         try:
-            h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            return int(pynvml.nvmlDeviceGetMemoryInfo(h).used)
-        finally:
-            pynvml.nvmlShutdown()
-    except Exception:
-        return None
+            pynvml.nvmlInit()
+            try:
+                h = pynvml.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}")
+                return int(pynvml.nvmlDeviceGetMemoryInfo(h).used)
+            finally:
+                pynvml.nvmlShutdown()
+        except Exception:
+            pass
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=memory.used", "--format=csv,noheader,nounits",
+                              "-i", f"GPU-{uuid}"], capture_output=True, text=True, timeout=20)
+        if out.returncode == 0 and out.stdout.strip():
+            return int(float(out.stdout.strip().splitlines()[0])) * 2**20
+    except (OSError, ValueError, subprocess.TimeoutExpired):
+        pass
+    return None
 
 
 def oracle_sample_rate(inp_cpu: dict, T: float, sample: int) -> dict:
@@ -285,9 +305,7 @@ def run_gpu(args):
     torch.cuda.reset_peak_memory_stats(dev)
     mem0 = torch.cuda.memory_allocated(dev)
     torch.cuda.synchronize(dev)
-    phys_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
-    nvml0 = nvml_used_bytes(phys_index)
+    nvml0 = nvml_used_bytes(dev)
     inp = workloads.make_inputs(cfg, seed=rank, device=dev)
     h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
     gh = torch.empty((N, H), dtype=torch.float32, device=dev)
@@ -310,7 +328,7 @@ def run_gpu(args):
     for _ in range(max(args.warmup, 3) if not args.allow_short_warmup else args.warmup):
         loss = step()
     peak_gib = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
-    nvml1 = nvml_used_bytes(phys_index)
+    nvml1 = nvml_used_bytes(dev)
     # cross-check: device memory NVML sees in use grew by (torch's reserved pool)
     nvml_delta_gib = (nvml1 - nvml0) / 2**30 if nvml0 is not None and nvml1 is not None else None
 
