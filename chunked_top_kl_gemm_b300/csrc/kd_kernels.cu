@@ -465,11 +465,14 @@ cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc,
 // the cached-id columns.  Both round exactly as the recompute GEMM's epilogue
 // does, so the two backward forms give bitwise the same dZ.
 __global__ void __launch_bounds__(256) kd_dz_from_z(const float* __restrict__ z, int V,
-                                                    int rows_valid, const float* __restrict__ lse2,
+                                                    int rows_valid, int col_blocks,
+                                                    const float* __restrict__ lse2,
                                                     float scale2, const uint8_t* __restrict__ mask,
                                                     int grow0, __nv_bfloat16* __restrict__ dz) {
-  const int r = blockIdx.y;
-  const int v = (blockIdx.x * 256 + threadIdx.x) * 8;
+  // one flat grid of rows x col_blocks (a chunk may hold more than 65,535 rows)
+  const int r = static_cast<int>(blockIdx.x / static_cast<unsigned>(col_blocks));
+  const int cb = static_cast<int>(blockIdx.x % static_cast<unsigned>(col_blocks));
+  const int v = (cb * 256 + threadIdx.x) * 8;
   if (v >= V) return;                       // V is a multiple of 8
   const long long off = static_cast<long long>(r) * V + v;
   uint4 out = make_uint4(0u, 0u, 0u, 0u);
@@ -512,9 +515,12 @@ __global__ void __launch_bounds__(256) kd_dz_fixup(const float* __restrict__ z, 
 cudaError_t launch_dz_from_z(const float* z, int V, int rows_valid, int rows_cover,
                              const float* lse2, float scale2, const uint8_t* mask, int grow0,
                              const int* sid, const float* sp, int K, void* dz, cudaStream_t s) {
-  dim3 grid((V / 8 + 255) / 256, rows_cover);
-  kd_dz_from_z<<<grid, 256, 0, s>>>(z, V, rows_valid, lse2, scale2, mask, grow0,
-                                    static_cast<__nv_bfloat16*>(dz));
+  const int col_blocks = (V / 8 + 255) / 256;
+  const long long blocks = static_cast<long long>(rows_cover) * col_blocks;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kd_dz_from_z<<<static_cast<unsigned>(blocks), 256, 0, s>>>(z, V, rows_valid, col_blocks, lse2,
+                                                             scale2, mask, grow0,
+                                                             static_cast<__nv_bfloat16*>(dz));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long n = static_cast<long long>(rows_valid) * K;
@@ -635,19 +641,23 @@ __global__ void __launch_bounds__(SEL_TAU_THREADS) kd_sel_tau(const float2* __re
   }
 }
 
-// Values >= tau0 of row blockIdx.y, columns of this block's segment of
-// FLT_THREADS x FLT_UNROLL float4s.  A list holds SEL_GCAP candidates; the
-// count goes on past it, so a count above SEL_GCAP marks an overflow.
+// Values >= tau0 of one row, columns of one segment of FLT_THREADS x
+// FLT_UNROLL float4s: block b takes row b / segs, segment b % segs (a flat
+// grid: a chunk may hold more than 65,535 rows).  A list holds SEL_GCAP
+// candidates; the count goes on past it, so a count above SEL_GCAP marks an
+// overflow.
 __global__ void __launch_bounds__(FLT_THREADS) kd_sel_filter(const float* __restrict__ z, int V,
+                                                             int segs,
                                                              const float* __restrict__ tau,
                                                              uint32_t* __restrict__ cnt,
                                                              unsigned long long* __restrict__ cand) {
-  const int r = blockIdx.y;
+  const int r = static_cast<int>(blockIdx.x / static_cast<unsigned>(segs));
+  const int seg = static_cast<int>(blockIdx.x % static_cast<unsigned>(segs));
   const int lane = threadIdx.x & 31;
   const float t0 = __ldg(tau + r);
   const float4* z4 = reinterpret_cast<const float4*>(z + static_cast<long long>(r) * V);
   const int V4 = V >> 2;                      // V is a multiple of 8
-  const int i0 = blockIdx.x * (FLT_THREADS * FLT_UNROLL) + threadIdx.x;
+  const int i0 = seg * (FLT_THREADS * FLT_UNROLL) + threadIdx.x;
   float4 x[FLT_UNROLL];
 #pragma unroll
   for (int u = 0; u < FLT_UNROLL; ++u) {
@@ -798,8 +808,10 @@ cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int V4 = V / 4;
-  dim3 fgrid((V4 + FLT_THREADS * FLT_UNROLL - 1) / (FLT_THREADS * FLT_UNROLL), rows_valid);
-  kd_sel_filter<<<fgrid, FLT_THREADS, 0, s>>>(z, V, tau, cnt, cand);
+  const int segs = (V4 + FLT_THREADS * FLT_UNROLL - 1) / (FLT_THREADS * FLT_UNROLL);
+  const long long fblocks = static_cast<long long>(rows_valid) * segs;
+  if (fblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kd_sel_filter<<<static_cast<unsigned>(fblocks), FLT_THREADS, 0, s>>>(z, V, segs, tau, cnt, cand);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kd_sel_sort<<<rows_valid, SORT_THREADS, 0, s>>>(cnt, cand, K, row0, out_idx, out_val);

@@ -90,6 +90,24 @@ def test_store_logits_full_vocabulary_two_chunks():
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
+def test_chunk_of_more_than_65535_rows():
+    """One 70,016-row chunk: the elementwise dZ kernel covers more rows than a
+    grid's y dimension could hold.  Equal to the recompute, and to the oracle
+    on sampled tokens."""
+    ensure_lib()
+    cfg = workloads.custom("z_big", N=70000, H=64, V=512, K=8, T=1.0, chunk=70000)
+    inp_cpu = workloads.make_inputs(cfg, seed=13)
+    inp = to_device(inp_cpu)
+    a = _run(inp, cfg.T, cfg.chunk, 0)
+    b = _run(inp, cfg.T, cfg.chunk, kd.KD_FLAG_STORE_LOGITS)
+    assert a[0] == b[0]
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    rows = np.array([0, 1, 65534, 65535, 65536, 69998, 69999])
+    want = oracle.rows_forward(inp_cpu["hidden"][rows], inp_cpu["W"], inp_cpu["topk_idx"][rows],
+                               inp_cpu["topk_logit"][rows], cfg.T, N_total=cfg.N)
+    assert rel_l2(b[1].cpu().numpy()[rows], want["grad_hidden"]) <= GRAD_REL_L2
+
+
 def test_workspace_grows_by_the_chunk_logits():
     ensure_lib()
     N, H, V, K, chunk = 32768, 2880, 201088, 100, 2048

@@ -98,6 +98,20 @@ def test_realistic_head_full_vocabulary():
     assert agree > 0.999
 
 
+def test_chunk_of_more_than_65535_rows():
+    """One 70,016-row chunk: the streaming filter covers more rows than a
+    grid's y dimension could hold.  Integer logits, so sampled rows must
+    equal the oracle's bit for bit."""
+    ensure_lib()
+    N, H, V, K = 70000, 32, 512, 8
+    h, W = _int_inputs(N, H, V, -2, 2, seed=17)
+    idx, val = _build(h, W, K, 70000)
+    rows = np.array([0, 1, 65534, 65535, 65536, 69998, 69999])
+    want = oracle.topk_cache(h[rows], W, K)
+    assert np.array_equal(idx[rows], want["topk_idx"])
+    assert np.array_equal(val[rows].astype(np.float64), want["topk_logit"])
+
+
 def test_cache_feeds_the_loss():
     """Build a cache from a teacher head, then run the loss against it."""
     ensure_lib()
