@@ -142,6 +142,13 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def _gpu_id(local: int) -> str:
+    """nvidia-smi's id of the GPU behind CUDA device `local`."""
+    if "CUDA_VISIBLE_DEVICES" in os.environ:
+        return os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]
+    return str(local)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -332,12 +339,11 @@ def run_gpu(args):
     # cross-check: device memory NVML sees in use grew by (torch's reserved pool)
     nvml_delta_gib = (nvml1 - nvml0) / 2**30 if nvml0 is not None and nvml1 is not None else None
 
-    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] \
-        if "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
+    gpu_id = _gpu_id(local)
+    # the headline: K steps with the library's per-kernel profiler off
     clocks = ClockSampler(gpu_id)
     clocks.start()
     time.sleep(0.5)
-    kd.kd_profile_enable(True)
     dist_barrier(dev)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -348,10 +354,28 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     dist_barrier(dev)
-    kd.kd_profile_enable(False)
     clk = clocks.stop()
-    prof = kd.kd_profile_read()
     t_dev = e0.elapsed_time(e1) / 1e3
+
+    # a second, labelled pass with the profiler on: every launch bracketed by
+    # two CUDA events on the launch stream (per-kernel times, the roofline of
+    # the dominant kernel and the launch count)
+    prof_steps = max(1, args.profile_steps or args.steps)
+    pclocks = ClockSampler(gpu_id)
+    pclocks.start()
+    time.sleep(0.2)
+    kd.kd_profile_enable(True)
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(prof_steps):
+        step()
+    p1.record(stream)
+    torch.cuda.synchronize(dev)
+    kd.kd_profile_enable(False)
+    pclk = pclocks.stop()
+    prof = kd.kd_profile_read()
+    t_prof = p0.elapsed_time(p1) / 1e3
     t_max = dist_max(t_dev, dev)
     value = throughput(N, args.steps, world, t_max)
     # the recompute path does four GEMMs of 2NHV; storing the logits skips one
@@ -409,11 +433,14 @@ def run_gpu(args):
     gemm = {k: prof[k] for k in GEMM_KINDS if k in prof and prof[k][1] > 0}
     dom = max(gemm, key=lambda k: gemm[k][0])
     dom_ms, dom_launches = gemm[dom]
-    flops_per_launch = 2.0 * N * H * V / (dom_launches / args.steps)
+    # the dominant GEMM's launches together do 2NHV flop per step
+    flops_per_launch = 2.0 * N * H * V / (dom_launches / prof_steps)
     achieved = flops_per_launch / (dom_ms / dom_launches / 1e3) / 1e12
     peak_sust = float(peaks["bf16_tflops_sustained"])
     traffic = stored_traffic(dom, cfg.name)
-    launches = sum(c for _, c in prof.values())
+    # the library's launches per step are fixed by the plan: the profiled
+    # pass counts them
+    launches_per_step = sum(c for _, c in prof.values()) / prof_steps
 
     cpu = None
     if world == 1 and not args.skip_cpu_baseline:
@@ -444,10 +471,14 @@ def run_gpu(args):
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})", "unit": "TFLOP/s",
                      "frac": achieved / peak_sust, "traffic": traffic,
                      "flops_per_launch": flops_per_launch,
-                     "avg_launch_ms": dom_ms / dom_launches},
-        "kernels": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                     "avg_launch_ms": dom_ms / dom_launches,
+                     "source": f"separate pass of {prof_steps} steps with the per-launch "
+                               "event profiler on (not the headline loop)"},
+        "kernels": {k: {"ms_per_step": v[0] / prof_steps, "launches_per_step": v[1] / prof_steps}
                     for k, v in prof.items() if v[1] > 0},
-        "gpu_launches": launches,
+        "profile_pass": {"steps": prof_steps, "ms_per_step": t_prof / prof_steps * 1e3,
+                         "clocks": pclk},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clk,
         "e2e": {"value": throughput(N, args.steps, world, t_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16},
@@ -510,7 +541,13 @@ def run_sweep(args):
         loss = kd.kd_topk_kl_fwd_bwd_ex(*args_)
         torch.cuda.synchronize(dev)
         peak = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
-        steps = max(1, min(args.steps, int(4e13 // cfg.flops) + 1))
+        # time one more warm call, then enough steps for ~1.5 s of samples
+        w0 = time.perf_counter()
+        kd.kd_topk_kl_fwd_bwd_ex(*args_)
+        steps = max(3, min(200, int(1.5 / max(time.perf_counter() - w0, 1e-4)) + 1))
+        clocks = ClockSampler(_gpu_id(0))
+        clocks.start()
+        time.sleep(0.2)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -518,6 +555,7 @@ def run_sweep(args):
             loss = kd.kd_topk_kl_fwd_bwd_ex(*args_)
         e1.record()
         torch.cuda.synchronize(dev)
+        clk = clocks.stop()
         t = e0.elapsed_time(e1) / 1e3 / steps
         tflops = cfg.flops / t / 1e12
         print(json.dumps({
@@ -530,7 +568,7 @@ def run_sweep(args):
             "grads_gib": 4 * (N * H + V * H) / 2**30,
             "workspace_gib": ws.numel() / 2**30,
             "dense_fp32_logits_gib": 4 * N * V / 2**30, "loss": loss,
-            "cpu_baseline": oracle_rate.get(name)}), flush=True)
+            "clocks": clk, "cpu_baseline": oracle_rate.get(name)}), flush=True)
         del inp, gh, gW, ws, args_
 
 
@@ -561,18 +599,26 @@ def run_cache_build(args):
 
     for _ in range(max(args.warmup, 3)):
         step()
-    kd.kd_profile_enable(True)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(_gpu_id(0))
+    clocks.start()
+    time.sleep(0.2)
     torch.cuda.synchronize(dev)
     e0.record()
     for _ in range(args.steps):
         step()
     e1.record()
     torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    # per-kernel split from a separate pass with the event profiler on
+    kd.kd_profile_enable(True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
     kd.kd_profile_enable(False)
     prof = kd.kd_profile_read()
-    t = e0.elapsed_time(e1) / 1e3 / args.steps
     peaks, _ = load_peaks()
     gemm_ms = prof["cache_gemm_logits"][0] / args.steps
     sel_ms = prof["cache_topk_select"][0] / args.steps
@@ -589,6 +635,8 @@ def run_cache_build(args):
         "select_gbs": 4.0 * N * V / (sel_ms / 1e3) / 1e9,
         "select_frac_hbm": 4.0 * N * V / (sel_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
         "kernels": {k: {"ms_per_step": v[0] / args.steps} for k, v in prof.items() if v[1]},
+        "kernels_source": "separate pass with the per-launch event profiler on",
+        "clocks": clk,
     }), flush=True)
 
 
@@ -607,6 +655,8 @@ def main(argv=None):
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--store-logits", action="store_true",
                     help="ablation: keep each chunk's logits instead of recomputing them")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="steps of the separate per-kernel profiling pass (default: --steps)")
     ap.add_argument("--allow-short-warmup", action="store_true",
                     help="profiling runs only: honour --warmup below 3")
     ap.add_argument("--sweep", action="store_true",

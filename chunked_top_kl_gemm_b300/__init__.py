@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
     L.kd_last_cuda_error.restype = ctypes.c_char_p
     L.kd_abi_version.argtypes = []
     L.kd_abi_version.restype = i32
+    L.kd_build_id.argtypes = []
+    L.kd_build_id.restype = ctypes.c_char_p
     L.kd_profile_enable.argtypes = [i32]
     L.kd_profile_enable.restype = None
     L.kd_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double),
@@ -104,8 +106,28 @@ def lib() -> ctypes.CDLL:
     L.kd_profile_read.restype = i32
     L.kd_profile_kind_name.argtypes = [i32]
     L.kd_profile_kind_name.restype = ctypes.c_char_p
+    _check_build_id(L)
     _lib = L
     return L
+
+
+def _check_build_id(L) -> None:
+    """Refuse a library built from other sources than the ones beside it
+    (it would run code that is not in the tree)."""
+    from . import _build
+    if not os.path.isdir(_build.CSRC):
+        return                      # installed without sources: nothing to compare
+    built = L.kd_build_id().decode()
+    want = _build.source_hash()
+    if built != want:
+        raise RuntimeError(
+            f"{LIB_PATH} was built from other sources (build id {built}, sources {want}): "
+            "rebuild it with `python -m chunked_top_kl_gemm_b300._build`")
+
+
+def build_id() -> str:
+    """The source hash compiled into the loaded library."""
+    return lib().kd_build_id().decode()
 
 
 def header_functions() -> list:

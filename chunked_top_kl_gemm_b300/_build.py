@@ -7,6 +7,7 @@ The library lands next to this file; the Python binding loads it from there.
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import shutil
 import subprocess
@@ -29,17 +30,40 @@ def nvcc() -> str:
 
 
 def _inputs():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))]
     files.append(os.path.join(INCLUDE, "kd_topk_kl.h"))
     files.append(os.path.abspath(__file__))
     return files
 
 
+def source_hash() -> str:
+    """SHA-256 (first 16 hex digits) of every file the library is built
+    from: the CUDA sources, the public header and this build script (its
+    flags).  The build compiles it into the library (``kd_build_id``)."""
+    h = hashlib.sha256()
+    for f in _inputs():
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def built_id(path: str = LIB):
+    """``kd_build_id()`` of the library at ``path``, asked in a child
+    process (this process may already hold another copy loaded), or None
+    when it cannot be loaded."""
+    if not os.path.exists(path):
+        return None
+    code = ("import ctypes,sys; L=ctypes.CDLL(sys.argv[1]); "
+            "L.kd_build_id.restype=ctypes.c_char_p; print(L.kd_build_id().decode())")
+    res = subprocess.run([sys.executable, "-c", code, path], capture_output=True, text=True)
+    return res.stdout.strip() if res.returncode == 0 else None
+
+
 def stale() -> bool:
-    if not os.path.exists(LIB):
-        return True
-    t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(f) > t for f in _inputs())
+    """True unless the library exists and was built from the sources as
+    they are now (by content, not by file times)."""
+    return built_id() != source_hash()
 
 
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
@@ -47,6 +71,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         return LIB
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
            "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
+           f"-DKD_BUILD_ID=\"{source_hash()}\"",
            "-o", LIB + ".tmp", *[os.path.join(CSRC, s) for s in SOURCES],
            *extra]
     if verbose:

@@ -753,7 +753,14 @@ void* noalloc_scratch(kd_status* st) {
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
+    // the first lookup on a device loads the module that holds the buffer
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaErrorMemoryAllocation) {
+      cuda_fail(e, "cudaGetSymbolAddress");
+      cudaGetLastError();
+      *st = KD_ERR_OOM;
+      return nullptr;
+    }
     if (e != cudaSuccess || p == nullptr) {
       *st = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "cudaGetSymbolAddress");
       return nullptr;
@@ -828,5 +835,10 @@ const char* kd_profile_kind_name(int kind) {
 }
 
 int kd_abi_version(void) { return 2; }
+
+#ifndef KD_BUILD_ID
+#define KD_BUILD_ID "unknown"
+#endif
+const char* kd_build_id(void) { return KD_BUILD_ID; }
 
 }  // extern "C"

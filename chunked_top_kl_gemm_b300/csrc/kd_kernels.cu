@@ -194,29 +194,36 @@ cudaError_t launch_gemm(int variant, const CUtensorMap& a, const CUtensorMap& b,
 // a_k = l_k / T, log p_k = a_k - logsumexp(a), p_k = exp(log p_k), in fp32
 // (single-precision exp/log), with the row sums sum_k p log p and sum_k p
 // accumulated in double.  Writes the row's ids sorted ascending (ties by
-// original position) with p and the original position alongside.  An id
-// outside [0, V) raises DEV_ERR_INDEX.
+// original position) with p and the original position alongside: the warp
+// sorts the keys (id << 32 | k) in shared memory with a bitonic network over
+// P >= K slots (padding keys sort last).  An id outside [0, V) raises
+// DEV_ERR_INDEX.
 __global__ void __launch_bounds__(256) kd_prep_topk(const int32_t* __restrict__ idx,
                                                     const float* __restrict__ logit, long long N,
-                                                    int K, int V, float invT,
+                                                    int K, int P, int V, float invT,
                                                     int* __restrict__ sid, float* __restrict__ sp,
                                                     int* __restrict__ perm,
                                                     double* __restrict__ ent,
                                                     double* __restrict__ psum, DevStatus* st) {
-  extern __shared__ int s_ids[];
+  extern __shared__ unsigned long long s_keys[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + warp;
   if (r >= N) return;
-  int* ids = s_ids + warp * K;
+  unsigned long long* keys = s_keys + static_cast<long long>(warp) * P;
   const int32_t* id_row = idx + r * K;
   const float* l_row = logit + r * K;
   float m = -CUDART_INF_F;
   bool bad = false;
-  for (int k = lane; k < K; k += 32) {
-    const int id = id_row[k];
-    ids[k] = id;
-    bad |= (id < 0) || (id >= V);
-    m = fmaxf(m, l_row[k] * invT);
+  for (int k = lane; k < P; k += 32) {
+    unsigned long long key = ~0ull;
+    if (k < K) {
+      const int id = id_row[k];
+      key = (static_cast<unsigned long long>(static_cast<uint32_t>(id)) << 32) |
+            static_cast<uint32_t>(k);
+      bad |= (id < 0) || (id >= V);
+      m = fmaxf(m, l_row[k] * invT);
+    }
+    keys[k] = key;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&st->err, DEV_ERR_INDEX);
 #pragma unroll
@@ -226,22 +233,12 @@ __global__ void __launch_bounds__(256) kd_prep_topk(const int32_t* __restrict__ 
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   const float lse_t = m + logf(s);
-  __syncwarp();
   double e_acc = 0.0, p_acc = 0.0;
   for (int k = lane; k < K; k += 32) {
     const float lp = l_row[k] * invT - lse_t;
     const float p = expf(lp);
     e_acc += static_cast<double>(p) * static_cast<double>(lp);
     p_acc += static_cast<double>(p);
-    const int idk = ids[k];
-    int rank = 0;
-    for (int j = 0; j < K; ++j) {
-      const int idj = ids[j];
-      rank += (idj < idk) || (idj == idk && j < k);
-    }
-    sid[r * K + rank] = idk;
-    sp[r * K + rank] = p;
-    perm[r * K + rank] = k;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -252,18 +249,53 @@ __global__ void __launch_bounds__(256) kd_prep_topk(const int32_t* __restrict__ 
     ent[r] = e_acc;
     psum[r] = p_acc;
   }
+  // ascending bitonic sort of keys[0..P)
+  __syncwarp();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = lane; i < P; i += 32) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const unsigned long long a = keys[i], b = keys[j];
+          if ((a > b) == ((i & size) == 0)) {
+            keys[i] = b;
+            keys[j] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  for (int q = lane; q < K; q += 32) {
+    const unsigned long long key = keys[q];
+    const int k = static_cast<int>(key & 0xffffffffu);
+    sid[r * K + q] = static_cast<int>(key >> 32);
+    sp[r * K + q] = expf(l_row[k] * invT - lse_t);
+    perm[r * K + q] = k;
+  }
 }
 
 cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N, int K, int V,
                              float T, int* sid, float* sp, int* perm, double* ent, double* psum,
                              DevStatus* st, cudaStream_t s) {
-  int wpb = 32768 / (K * 4);
+  int P = 32;
+  while (P < K) P <<= 1;                       // K <= 8192: P <= 8192, 64 KB of keys
+  int wpb = 65536 / (P * 8);
   wpb = wpb < 1 ? 1 : (wpb > 8 ? 8 : wpb);
+  const size_t smem = static_cast<size_t>(wpb) * P * 8;
+  static bool attr_set[64] = {};  // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kd_prep_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   const long long blocks = (N + wpb - 1) / wpb;
-  const size_t smem = static_cast<size_t>(wpb) * K * 4;
   kd_prep_topk<<<static_cast<unsigned>(blocks), wpb * 32, smem, s>>>(
-      idx, logit, N, K, V, static_cast<float>(1.0 / static_cast<double>(T)), sid, sp, perm, ent,
-      psum, st);
+      idx, logit, N, K, P, V, static_cast<float>(1.0 / static_cast<double>(T)), sid, sp, perm,
+      ent, psum, st);
   return cudaGetLastError();
 }
 
@@ -506,6 +538,7 @@ __global__ void __launch_bounds__(256) kd_dz_fixup(const float* __restrict__ z, 
   const int* ids = sid + g * K;
   const float* ps = sp + g * K;
   const int id = ids[k];
+  if (id < 0 || id >= V) return;             // out of range: the call reports KD_ERR_INDEX
   if (k > 0 && ids[k - 1] == id) return;     // the run's first entry writes
   float val = ex2_approx(fmaf(z[static_cast<long long>(r) * V + id], scale2, -lse2[r]));
   for (int j = k; j < K && ids[j] == id; ++j) val -= ps[j];

@@ -304,8 +304,8 @@ const char* kd_profile_kind_name(int kind);
 
 /*
  * Size of the library's built-in scratch buffer used by
- * kd_topk_kl_fwd_bwd_noalloc (64 MiB, held on every device that loads the
- * library until the process exits).
+ * kd_topk_kl_fwd_bwd_noalloc (64 MiB on each device, from the first call
+ * on that device until the process exits).
  */
 #define KD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -328,7 +328,12 @@ const char* kd_profile_kind_name(int kind);
  *    vocabulary at chunk 128 and 4,096 tokens does not.
  *  - The first call on a device looks up the buffer's device address on the
  *    current device (cudaGetSymbolAddress); make that first call before any
- *    stream capture.
+ *    stream capture.  CUDA loads a library's device code, and with it this
+ *    buffer, when it is first used on a device, so the 64 MiB are taken
+ *    from the device at that first call: a caller whose memory pool will
+ *    take the rest of the device makes one call (any valid size) before the
+ *    pool reserves it.  If the device cannot hold the buffer then, the call
+ *    returns KD_ERR_OOM.
  *  - The buffer is shared by every call on a device and keeps the previous
  *    call's contents; each call resets what must start at zero.  Calls whose
  *    work overlaps on the GPU (several streams or threads at once) race on
@@ -350,6 +355,12 @@ const char* kd_last_cuda_error(void);
 
 /* Version of this ABI (incremented on any incompatible change). */
 int kd_abi_version(void);
+
+/* Identity of the sources this library was built from: the first 16 hex
+ * digits of a SHA-256 over the CUDA sources, this header and the build
+ * script, fixed at compile time ("unknown" for a build that did not set
+ * it).  Static text. */
+const char* kd_build_id(void);
 
 #ifdef __cplusplus
 }

@@ -24,6 +24,12 @@ def test_every_declared_function_is_exported(L):
         assert hasattr(L, name), name
 
 
+def test_library_is_built_from_the_sources_in_the_tree(L):
+    # the build id compiled into the library is the hash of the sources now
+    assert kd.build_id() == _build.source_hash()
+    assert not _build.stale()
+
+
 def test_status_strings(L):
     for code in range(8):
         assert kd.kd_status_string(code)

@@ -37,6 +37,26 @@ def test_out_of_range_id_is_reported(bad):
     assert ei.value.name == "KD_ERR_INDEX"
 
 
+@pytest.mark.parametrize("bad", [-1, 512, 1 << 30])
+def test_out_of_range_id_is_reported_with_stored_logits(bad):
+    # the stored-logits backward rewrites dZ at the cached ids; it skips an
+    # id outside [0, V) instead of addressing the logits with it
+    inp = _inputs()
+    inp["topk_idx"][150, 0] = bad
+    N, H = inp["hidden"].shape
+    V, K = inp["W"].shape[0], inp["topk_idx"].shape[1]
+    flags = kd.KD_FLAG_STORE_LOGITS
+    ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, CFG.chunk, flags),
+                     dtype=torch.uint8, device="cuda")
+    gh = torch.empty((N, H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+    with pytest.raises(kd.KdError) as ei:
+        kd.kd_topk_kl_fwd_bwd_flags(inp["hidden"], inp["W"], inp["topk_idx"],
+                                    inp["topk_logit"], None, CFG.T, CFG.chunk, flags, gh, gW, ws)
+    assert ei.value.name == "KD_ERR_INDEX"
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("site", [1, 2, 3, 4], ids=["fwd", "recompute", "grad_hidden", "grad_W"])
 def test_injected_wait_times_out_and_context_survives(site):
     # each GEMM kind (its epilogue, staging and stores) takes the abort and
