@@ -317,14 +317,15 @@ def run_gpu(args):
     h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
     gh = torch.empty((N, H), dtype=torch.float32, device=dev)
     gW = torch.empty((V, H), dtype=torch.float32, device=dev)
-    flags = kd.KD_FLAG_STORE_LOGITS if args.store_logits else 0
+    flags = (kd.KD_FLAG_STORE_LOGITS if args.store_logits else 0) | \
+        (kd.KD_FLAG_MIN_SCRATCH if args.min_scratch else 0)
     ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, flags),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
     del inp
 
-    if args.store_logits:
+    if flags:
         def step():
             return kd.kd_topk_kl_fwd_bwd_flags(h, W, idx, lg, None, T, chunk, flags, gh, gW, ws,
                                                stream=stream)
@@ -408,7 +409,7 @@ def run_gpu(args):
             if i + 1 < n:
                 copy_in(1 - slot)   # the other buffers are free: their step has returned
             hb, ib, lb = bufs[slot]
-            if args.store_logits:
+            if flags:
                 kd.kd_topk_kl_fwd_bwd_flags(hb, W, ib, lb, None, T, chunk, flags, gh, gW, ws,
                                             stream=stream)
             else:
@@ -460,6 +461,8 @@ def run_gpu(args):
                    "chunk": chunk, "parallelism": f"replicas{world}" if world > 1 else "single",
                    "backward": "stored fp32 logits (6NHV)" if args.store_logits
                                else "recompute (8NHV)",
+                   "grad_W_depth": "one chunk (minimal scratch)" if args.min_scratch
+                                   else "two chunks",
                    "l2": "inputs larger than L2 (W is 1.16 GB and is streamed every GEMM)"},
         "tflops": tflops,
         "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
@@ -657,6 +660,8 @@ def main(argv=None):
                     help="ablation: keep each chunk's logits instead of recomputing them")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="steps of the separate per-kernel profiling pass (default: --steps)")
+    ap.add_argument("--min-scratch", action="store_true",
+                    help="one chunk's dZ in the workspace: grad_W formed per chunk")
     ap.add_argument("--allow-short-warmup", action="store_true",
                     help="profiling runs only: honour --warmup below 3")
     ap.add_argument("--sweep", action="store_true",

@@ -27,6 +27,7 @@ KD_ERR_INDEX = 3
 KD_ERR_TIMEOUT = 6
 KD_FLAG_ACCUMULATE = 1
 KD_FLAG_STORE_LOGITS = 2
+KD_FLAG_MIN_SCRATCH = 4
 STATUS_NAMES = {
     0: "KD_OK", 1: "KD_ERR_INVALID_ARG", 2: "KD_ERR_ALIGNMENT", 3: "KD_ERR_INDEX",
     4: "KD_ERR_OOM", 5: "KD_ERR_CUDA", 6: "KD_ERR_TIMEOUT", 7: "KD_ERR_NOT_IMPLEMENTED",

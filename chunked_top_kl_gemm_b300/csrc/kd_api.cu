@@ -29,6 +29,7 @@ kd_status cuda_fail(cudaError_t e, const char* where) {
 
 constexpr uint64_t kDefaultTimeoutNs = 5ull * 1000 * 1000 * 1000;
 constexpr int kMaxK = 8192;
+constexpr unsigned kAllFlags = KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS | KD_FLAG_MIN_SCRATCH;
 
 // ---------------------------------------------------------------- profiler
 // Optional per-kernel timing: when enabled, every launch of run() is
@@ -157,6 +158,7 @@ struct Plan {
   int mth;        // hidden tiles (M) of the grad_hidden^T GEMM
   int hp;         // mth * its tile M: rows of one split's grad_hidden^T partial
   int splits;     // K splits of the grad_hidden^T GEMM
+  int gg;         // chunks whose dZ one grad_W GEMM reduces over (1 or 2)
   int sms;
   bool store_z;   // keep each chunk's fp32 logits instead of recomputing them
   size_t off_status, off_sid, off_sp, off_perm, off_ent, off_psum, off_loss_rows, off_lse2,
@@ -190,7 +192,12 @@ int pick_splits(int units, int kb_total, int sms) {
   return best;
 }
 
-Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_z = false) {
+// The grad_W GEMM reduces over the dZ rows of gg consecutive chunks at once
+// (K = gg x chunk): its fp32 read-modify-write of all of grad_W, 8 V H bytes
+// per launch, then happens once per gg chunks.  gg = 2 holds two chunks' dZ
+// (2 x chunk x V bf16); KD_FLAG_MIN_SCRATCH keeps one (gg = 1).
+Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_z = false,
+               bool min_scratch = false) {
   Plan p{};
   p.N = N; p.H = H; p.V = V; p.K = K; p.sms = sms; p.store_z = store_z;
   long long c = cdiv(chunk, 128) * 128;
@@ -198,6 +205,7 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_
   if (c > cmax) c = cmax;
   p.chunk = static_cast<int>(c);
   p.n_chunks = static_cast<int>(cdiv(N, c));
+  p.gg = (min_scratch || p.n_chunks < 2) ? 1 : 2;
   p.vt = static_cast<int>(cdiv(V, kd::gemm_bn(kd::GV_FWD)));
   p.ht = static_cast<int>(cdiv(H, kd::gemm_bn(kd::GV_GRAD_W)));
   p.mth = static_cast<int>(cdiv(H, kd::gemm_tile_m(kd::GV_GRAD_H)));
@@ -216,9 +224,9 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_
   p.off_lse2 = take(sizeof(float) * c);
   p.off_zg = take(sizeof(float) * c * K);
   p.off_part = take(sizeof(float2) * p.vt * c);
-  p.off_dz = take(2ull * c * V);
+  p.off_dz = take(2ull * p.gg * c * V);
   p.off_k4 = take(4ull * p.splits * p.hp * c);
-  p.off_hT = take(2ull * H * c);
+  p.off_hT = take(2ull * H * p.gg * c);
   p.off_z = store_z ? take(4ull * c * V) : 0;
   p.total = o;
   return p;
@@ -273,7 +281,8 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   const bool async = loss_dev != nullptr;
   const int accumulate = (flags & KD_FLAG_ACCUMULATE) ? 1 : 0;
   const bool store_z = (flags & KD_FLAG_STORE_LOGITS) != 0;
-  if (flags & ~(KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS)) return KD_ERR_INVALID_ARG;
+  const bool min_scratch = (flags & KD_FLAG_MIN_SCRATCH) != 0;
+  if (flags & ~kAllFlags) return KD_ERR_INVALID_ARG;
   kd_status st = validate(hidden, W, idx, logit, N, H, V, K, T, chunk, async ? loss_dev : loss,
                           gh, gW);
   if (st != KD_OK) return st;
@@ -283,7 +292,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     if (!aligned(loss_dev, 4) || !aligned(status_dev, 4)) return KD_ERR_ALIGNMENT;
     if (!is_device_ptr(loss_dev) || !is_device_ptr(status_dev)) return KD_ERR_INVALID_ARG;
   }
-  const Plan p = make_plan(N, H, V, K, chunk, device_sms(), store_z);
+  const Plan p = make_plan(N, H, V, K, chunk, device_sms(), store_z, min_scratch);
   if (!ws || ws_bytes < p.total) return KD_ERR_OOM;
   prof().used = 0;
   if (!aligned(ws, 256)) return KD_ERR_ALIGNMENT;
@@ -318,12 +327,13 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   bool ok = true;
   ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
   ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, b_box_rows(kd::GV_FWD));
-  ok &= make_map(&tm_dz_st, BF16, 2, dz, V, p.chunk, 64, 32);
-  ok &= make_map(&tm_dz_k256, BF16, 2, dz, V, p.chunk, 64, b_box_rows(kd::GV_GRAD_H));
+  const uint64_t dz_rows = static_cast<uint64_t>(p.gg) * p.chunk;   // dZ of gg chunks
+  ok &= make_map(&tm_dz_st, BF16, 2, dz, V, dz_rows, 64, 32);
+  ok &= make_map(&tm_dz_k256, BF16, 2, dz, V, dz_rows, 64, b_box_rows(kd::GV_GRAD_H));
   ok &= make_map(&tm_w_mn, BF16, 2, W, H, V, 64, 64);
   ok &= make_map(&tm_k4_st, F32, 4, k4, p.chunk, static_cast<uint64_t>(p.splits) * p.hp, 32, 32);
-  ok &= make_map(&tm_dz_mn, BF16, 2, dz, V, p.chunk, 64, 64);
-  ok &= make_map(&tm_ht_k, BF16, 2, hT, p.chunk, H, 64, b_box_rows(kd::GV_GRAD_W));
+  ok &= make_map(&tm_dz_mn, BF16, 2, dz, V, dz_rows, 64, 64);
+  ok &= make_map(&tm_ht_k, BF16, 2, hT, dz_rows, H, 64, b_box_rows(kd::GV_GRAD_W));
   ok &= make_map(&tm_gw, F32, 4, gW, H, V, 32, 32);
   CUtensorMap tm_z_st;
   if (store_z) ok &= make_map(&tm_z_st, F32, 4, zbuf, V, p.chunk, 32, 32);
@@ -349,6 +359,10 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     const int row0 = j * p.chunk;
     const int cj = static_cast<int>(std::min<long long>(p.chunk, N - row0));
     const int mt = static_cast<int>(cdiv(cj, kd::gemm_tile_m(kd::GV_FWD)));
+    // this chunk's dZ rows and h_c^T columns: slot `slot` of its grad_W group
+    const int slot = j % p.gg;
+    const int slot_row0 = slot * p.chunk;
+    uint8_t* dz_slot = static_cast<uint8_t*>(dz) + 2ull * slot_row0 * V;
 
     kd::GemmArgs g{};
     g.m_tiles = mt; g.n_tiles = p.vt; g.splits = 1;
@@ -377,8 +391,10 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
       // rows up to the GEMMs' reach get a dZ row (zeros past the chunk)
       const int cover = static_cast<int>(std::min<long long>(p.chunk, cdiv(cj, 256) * 256));
       ProfScope ps_(PK_DZ_EW, s);
-      KD_CUDA(kd::launch_dz_from_z(zbuf, V, cj, cover, lse2, scale2, mask, row0, sid, sp, K, dz, s));
+      KD_CUDA(kd::launch_dz_from_z(zbuf, V, cj, cover, lse2, scale2, mask, row0, sid, sp, K,
+                                   dz_slot, s));
     } else {
+      e.out_row0 = slot_row0;                        // dZ rows of this chunk's slot
       ProfScope ps_(PK_DZ, s);
       KD_CUDA(kd::launch_gemm(kd::GV_DZ, tm_hid_k, tm_w_k, tm_dz_st, g, e, s));
     }
@@ -389,7 +405,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     g2.m_tiles = p.mth; g2.n_tiles = static_cast<int>(cdiv(cj, kd::gemm_bn(kd::GV_GRAD_H)));
     g2.splits = p.splits;
     g2.kb_total = static_cast<int>(cdiv(V, 64));
-    g2.order = kd::ORDER_SPLIT; g2.a_row0 = 0; g2.b_row0 = 0;
+    g2.order = kd::ORDER_SPLIT; g2.a_row0 = 0; g2.b_row0 = slot_row0;
     g2.timeout_ns = timeout; g2.status = dst; g2.inject_timeout = (j == 0 && inject == 3);
     kd::EpiArgs e2{};
     e2.rows_valid = H; e2.cols_valid = cj; e2.alpha = 1.f; e2.out_row0 = 0;
@@ -399,19 +415,24 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
                                     static_cast<long long>(p.hp) * p.chunk, p.chunk, cj, H, alpha, alpha_dev, accumulate,
                                     gh + static_cast<long long>(row0) * H, s)); }
 
-    // grad_W += dZ^T h_c   (B operand: h_c^T, K-major)
+    // h_c^T (B operand of grad_W, K-major) into the slot's columns
     { ProfScope ps_(PK_TRANSPOSE, s); KD_CUDA(kd::launch_transpose_chunk(
-          static_cast<const uint8_t*>(hidden) + 2ull * row0 * H, cj, p.chunk, H, hT, s)); }
+          static_cast<const uint8_t*>(hidden) + 2ull * row0 * H, cj, p.chunk, H,
+          static_cast<uint8_t*>(hT) + 2ull * slot_row0, static_cast<int>(dz_rows), s)); }
+
+    // grad_W += dZ_g^T h_g over the group's rows, once its last chunk is in
+    if (slot + 1 < p.gg && j + 1 < p.n_chunks) continue;
+    const int grp_rows = slot_row0 + cj;   // only the call's last chunk is partial
     kd::GemmArgs g3{};
     g3.m_tiles = static_cast<int>(cdiv(V, kd::gemm_tile_m(kd::GV_GRAD_W))); g3.n_tiles = p.ht;
     g3.splits = 1;
-    g3.kb_total = static_cast<int>(cdiv(cj, 64));
+    g3.kb_total = static_cast<int>(cdiv(grp_rows, 64));
     g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = 0;
-    g3.timeout_ns = timeout; g3.status = dst; g3.inject_timeout = (j == 0 && inject == 4);
+    g3.timeout_ns = timeout; g3.status = dst; g3.inject_timeout = (j == p.gg - 1 && inject == 4);
     kd::EpiArgs e3{};
     e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
     e3.alpha_dev = alpha_dev;
-    e3.first = (j == 0) && !accumulate;
+    e3.first = (j - slot == 0) && !accumulate;
     { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_ht_k, tm_gw, g3, e3, s)); }
   }
   kd::FinalOut fo{};
@@ -480,8 +501,9 @@ kd_status kd_topk_kl_fwd_bwd_masked(const void* hidden, const void* W, const int
 size_t kd_topk_kl_workspace_size_flags(int64_t N, int H, int V, int K, int chunk,
                                        unsigned flags) {
   if (!sizes_ok(N, H, V, K, chunk)) return 0;
-  if (flags & ~(KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS)) return 0;
-  return make_plan(N, H, V, K, chunk, device_sms(), (flags & KD_FLAG_STORE_LOGITS) != 0).total;
+  if (flags & ~kAllFlags) return 0;
+  return make_plan(N, H, V, K, chunk, device_sms(), (flags & KD_FLAG_STORE_LOGITS) != 0,
+                   (flags & KD_FLAG_MIN_SCRATCH) != 0).total;
 }
 
 kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int32_t* topk_idx,

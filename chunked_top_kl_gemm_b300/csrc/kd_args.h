@@ -28,7 +28,7 @@ struct EpiArgs {
   int cols_valid;        // valid columns of the N dimension
   float scale2;          // log2(e) / T
   float alpha;           // EPI_F32 / EPI_ACC scale
-  int out_row0;          // EPI_F32 / EPI_ACC: y offset of the output coordinates
+  int out_row0;          // EPI_F32 / EPI_ACC / EPI_DZ: y offset of the output coordinates
   int split_rows;        // EPI_F32: y offset between the outputs of two K splits
   int first;             // EPI_ACC: store instead of add
   // EPI_FWD / EPI_DZ

@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, box_row0);
+            tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, e.out_row0 + box_row0);
             bulk_commit();
           }
           ++sub_ctr;

@@ -82,8 +82,9 @@ cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_
 cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStatus* st,
                               cudaStream_t s);
 
+// hT[h * ld + r] = hid[r][h] for the chunk's rows (zeros up to c_alloc)
 cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
-                                   cudaStream_t s);
+                                   int ld, cudaStream_t s);
 
 // Device-side results of an asynchronous call (loss == nullptr: none).
 struct FinalOut {

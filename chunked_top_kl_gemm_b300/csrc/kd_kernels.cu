@@ -448,10 +448,13 @@ cudaError_t launch_split_reduce_t(const float* part, int splits, long long split
 }
 
 // ------------------------------------------------------------------ chunk transpose
-// hT[h][r] = hidden[r][h] for r < rows_valid, 0 for rows_valid <= r < c_alloc
-// (bf16; 64 x 64 tiles through shared memory, two elements per access).
+// hT[h * ld + r] = hidden[r][h] for r < rows_valid, 0 for rows_valid <= r <
+// c_alloc (bf16; 64 x 64 tiles through shared memory, two elements per
+// access).  ld >= c_alloc is the row length of the whole h^T buffer, which
+// holds the columns of several chunks.
 __global__ void __launch_bounds__(256) kd_transpose_chunk(const __nv_bfloat16* __restrict__ hid,
                                                           int rows_valid, int c_alloc, int H,
+                                                          int ld,
                                                           __nv_bfloat16* __restrict__ hT) {
   __shared__ __nv_bfloat16 tile[64][64 + 2];
   const int r0 = blockIdx.x * 64, h0 = blockIdx.y * 64;
@@ -477,16 +480,16 @@ __global__ void __launch_bounds__(256) kd_transpose_chunk(const __nv_bfloat16* _
       __nv_bfloat162 v;
       v.x = tile[r2][hh];
       v.y = tile[r2 + 1][hh];
-      *reinterpret_cast<__nv_bfloat162*>(hT + static_cast<long long>(h) * c_alloc + r) = v;
+      *reinterpret_cast<__nv_bfloat162*>(hT + static_cast<long long>(h) * ld + r) = v;
     }
   }
 }
 
 cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
-                                   cudaStream_t s) {
+                                   int ld, cudaStream_t s) {
   dim3 grid((c_alloc + 63) / 64, (H + 63) / 64);
   kd_transpose_chunk<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hid), rows_valid,
-                                          c_alloc, H, static_cast<__nv_bfloat16*>(hT));
+                                          c_alloc, H, ld, static_cast<__nv_bfloat16*>(hT));
   return cudaGetLastError();
 }
 

@@ -148,11 +148,20 @@ kd_status kd_topk_kl_fwd_bwd_masked(const void* hidden, const void* W, const int
 /* Flags of kd_topk_kl_fwd_bwd_flags / kd_topk_kl_workspace_size_flags. */
 #define KD_FLAG_ACCUMULATE 1u     /* add into grad_hidden / grad_W instead of overwriting */
 #define KD_FLAG_STORE_LOGITS 2u   /* keep each chunk's logits between forward and backward */
+#define KD_FLAG_MIN_SCRATCH 4u    /* one chunk's dZ in the workspace instead of two (see below) */
 
 /*
  * Workspace bytes for kd_topk_kl_fwd_bwd_flags with these flags (0 when the
  * sizes or the flags are invalid).  KD_FLAG_STORE_LOGITS adds chunk x V x 4
  * bytes (the chunk's fp32 logits).
+ *
+ * By default a call with two or more chunks keeps the bf16 dZ of two
+ * consecutive chunks (2 x chunk x V x 2 bytes) and forms grad_W once per
+ * pair of chunks, reducing over both chunks' rows at once: the fp32
+ * read-modify-write of all of grad_W (V x H x 8 bytes) then happens once per
+ * two chunks instead of once per chunk.  KD_FLAG_MIN_SCRATCH keeps one
+ * chunk's dZ (chunk x V x 2 bytes) and forms grad_W per chunk.  Both give
+ * the same result up to the fp32 rounding of grad_W's accumulation order.
  */
 size_t kd_topk_kl_workspace_size_flags(int64_t N, int H, int V, int K, int chunk,
                                        unsigned flags);
@@ -322,10 +331,11 @@ const char* kd_profile_kind_name(int kind);
  *
  *  - Sizes whose kd_topk_kl_workspace_size() exceeds KD_NOALLOC_SCRATCH_BYTES
  *    are rejected with KD_ERR_TOO_LARGE before anything is launched.  The
- *    scratch grows with chunk x V (the bf16 dZ of one chunk) and N x K (the
- *    sorted teacher tables); for example N = 4096, H = 4096, V = 32,000,
- *    K = 100 fits at chunk 256 (about 59 MiB), while a 201,088-token
- *    vocabulary at chunk 128 and 4,096 tokens does not.
+ *    scratch grows with chunk x V (the bf16 dZ of one chunk, or of two when
+ *    the call has two chunks or more) and N x K (the sorted teacher tables);
+ *    for example N = 4096, H = 4096, V = 32,000, K = 100 fits at chunk 128
+ *    (about 41 MiB), while a 201,088-token vocabulary at chunk 128 and 4,096
+ *    tokens does not.
  *  - The first call on a device looks up the buffer's device address on the
  *    current device (cudaGetSymbolAddress); make that first call before any
  *    stream capture.  CUDA loads a library's device code, and with it this

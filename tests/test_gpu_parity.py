@@ -43,6 +43,11 @@ CASES = {
     # larger head, several vocab and hidden tiles, chunk of 256 rows
     "mid": workloads.custom("mid", N=640, H=576, V=8192, K=100, T=1.0, chunk=256,
                             hidden_rms_norm=True, teacher="zipf"),
+    # grad_W reduces over pairs of chunks: 4 chunks, the second pair's second
+    # chunk ragged (50 rows); 5 chunks, the last (1 row) alone in its pair
+    "pairs_ragged_second": workloads.custom("pr2", N=434, H=136, V=1032, K=9, T=1.0,
+                                            chunk=128),
+    "pairs_lone_last": workloads.custom("pr1", N=513, H=136, V=1032, K=9, T=0.8, chunk=128),
 }
 
 
@@ -130,3 +135,40 @@ def test_spec_entry_point_matches_debug_entry_point():
     torch.cuda.synchronize()
     assert loss2 == ref["loss"]
     assert np.array_equal(gW2.cpu().numpy(), ref["grad_W"])
+
+
+@pytest.mark.parametrize("name", ["ragged", "pairs_ragged_second", "pairs_lone_last", "mid"])
+def test_grad_W_over_chunk_pairs_matches_per_chunk(name):
+    # default plan: grad_W reduces over two chunks' dZ at once; with
+    # KD_FLAG_MIN_SCRATCH it is formed per chunk.  The loss and grad_hidden
+    # do not depend on that (bitwise equal), grad_W only through the fp32
+    # accumulation order; both match the oracle.
+    import chunked_top_kl_gemm_b300 as kd
+    cfg = CASES[name]
+    ensure_lib()
+    inp_cpu = workloads.make_inputs(cfg, seed=9)
+    inp = to_device(inp_cpu)
+    N, H, V, K = cfg.N, cfg.H, cfg.V, cfg.K
+    res = {}
+    for flags in (0, kd.KD_FLAG_MIN_SCRATCH):
+        ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, cfg.chunk, flags),
+                         dtype=torch.uint8, device="cuda")
+        gh = torch.full((N, H), float("nan"), dtype=torch.float32, device="cuda")
+        gW = torch.full((V, H), float("nan"), dtype=torch.float32, device="cuda")
+        loss = kd.kd_topk_kl_fwd_bwd_flags(inp["hidden"], inp["W"], inp["topk_idx"],
+                                           inp["topk_logit"], None, cfg.T, cfg.chunk, flags,
+                                           gh, gW, ws)
+        torch.cuda.synchronize()
+        res[flags] = (loss, gh.cpu().numpy(), gW.cpu().numpy(), ws.numel())
+    a, b = res[0], res[kd.KD_FLAG_MIN_SCRATCH]
+    if -(-N // cfg.chunk) >= 2:
+        assert a[3] > b[3]                      # two chunks' dZ instead of one
+    assert a[0] == b[0]
+    assert np.array_equal(a[1], b[1])
+    assert rel_l2(a[2], b[2]) < 1e-5
+    want = oracle.fused_topk_kl(inp_cpu["hidden"], inp_cpu["W"], inp_cpu["topk_idx"],
+                                inp_cpu["topk_logit"], cfg.T)
+    for r in (a, b):
+        assert abs(r[0] - want["loss"]) <= 1e-3 * abs(want["loss"])
+        assert rel_l2(r[1], want["grad_hidden"]) <= 2e-2
+        assert rel_l2(r[2], want["grad_W"]) <= 2e-2
