@@ -68,8 +68,8 @@ def to_f64(x) -> np.ndarray:
         pass
     a = np.asarray(x)
     if np.issubdtype(a.dtype, np.integer):
-        return a.astype(np.int64)
-    return a.astype(np.float64)
+        return np.asarray(a, dtype=np.int64)
+    return np.asarray(a, dtype=np.float64)   # no copy when already float64
 
 
 def _logsumexp_rows(a: np.ndarray) -> np.ndarray:
@@ -173,21 +173,31 @@ def fused_topk_kl(hidden, W, topk_idx, topk_logit, T: float,
 
 
 def rows_forward(hidden_rows, W, idx_rows, logit_rows, T: float,
-                 N_total: int) -> dict:
+                 N_total: int, vrows=None, grad_hidden: bool = True) -> dict:
     """Per-token quantities for a subset of token rows.
 
     Every per-token output (its loss term, lse, gathered logits and its row
     of grad_hidden) depends only on that token's inputs and W, so a sample
     of rows can be checked at any N.  ``N_total`` is the token count of the
     full problem (the mean's denominator).
+
+    With ``vrows`` (vocabulary ids) the result also holds ``grad_W_rows``:
+    these tokens' share sum_n dZ_nv h_n of grad_W rows ``vrows``.  grad_W
+    is a sum over tokens, so the shares of disjoint token blocks add up to
+    the rows of the full problem's grad_W.  ``grad_hidden=False`` skips
+    the grad_hidden product (half the work of a block).
     """
     h = to_f64(hidden_rows)
     Wd = to_f64(W)
     idx = to_f64(idx_rows)
     lg = to_f64(logit_rows)
     _, lse, zg, lrow, D = _block_terms(h, Wd, idx, lg, T, N_total)
-    return {"lse": lse, "zg": zg, "loss_rows": lrow,
-            "grad_hidden": D @ Wd}
+    out = {"lse": lse, "zg": zg, "loss_rows": lrow}
+    if grad_hidden:
+        out["grad_hidden"] = D @ Wd
+    if vrows is not None:
+        out["grad_W_rows"] = D[:, np.asarray(vrows, dtype=np.int64)].T @ h
+    return out
 
 
 def grad_W_rows(hidden, W, topk_idx, topk_logit, T: float, vrows,

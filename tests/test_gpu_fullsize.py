@@ -1,23 +1,31 @@
 """The CUDA path at the workloads' full sizes, in the benchmark's launch configuration.
 
 Each workload (llama3b, gptoss32k, long64k, ext256k) runs whole on the GPU
-with its own chunk size, exactly as ``bench.py`` times it.  The float64
-oracle cannot redo a full call in seconds, so the checks are:
+with its own N, H, V, K, T and chunk, exactly as ``bench.py`` times it.
+Its inputs come from ``workloads.make_inputs_host`` (numpy's PCG64, the
+same bytes on every host), so the float64 oracle's values for the whole
+problem, computed once on the host by ``tests/golden/make_fullsize.py``
+(which calls only ``oracle/`` and ``workloads/``), apply to this run; the
+stored input digest proves the inputs are the same.  Checked against the
+oracle:
 
-* every gathered id on every row equals the cached id (bit-exact);
-* lse, gathered z, the per-token loss terms and grad_hidden of sampled
-  tokens against the oracle's ``rows_forward`` (each token's outputs depend
-  only on its own inputs and W);
-* the loss is the mean of the per-token terms;
-* grad_W through properties that hold at any size: its rows sum to zero
-  (softmax minus a distribution sums to zero over the vocabulary), and
-  <grad_W, W> = <grad_hidden, hidden>, both being sum_{n,v} dZ_nv z_nv;
-* a 256-token run at full H and V whose sampled grad_W rows (and all other
-  outputs) are compared with the oracle in full.
+* the mean loss over all N tokens (relative 1e-3);
+* every token's logsumexp and KL term;
+* grad_W on the stored vocabulary rows (teacher-hit ids, the last vocabulary
+  tile's boundary and end, random ids), each summing over all N tokens and
+  so over every chunk's reduce-add (relative L2 2e-2);
+* gathered z and grad_hidden of sampled tokens (``oracle.rows_forward``,
+  computed here);
+* at llama3b, all of grad_hidden and grad_W against the dense oracle run
+  here on the host cores.
 
-Inputs are drawn on the GPU with the workload's recipe; the oracle reads
-the same bf16 / int32 / fp32 values copied back to the host.
+Also: every gathered id on every row equals the cached id (bit-exact), the
+loss is the mean of the per-token terms, and grad_W satisfies two
+identities that hold at any size (its vocabulary rows sum to zero;
+<grad_W, W> = <grad_hidden, hidden>).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -30,7 +38,15 @@ from tests.gpu_util import (GRAD_REL_L2, LOSS_RTOL, LSE_ATOL, ZG_RTOL, assert_pa
 
 pytestmark = pytest.mark.gpu
 
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+FULL_SIZE = ["llama3b", "gptoss32k", "long64k", "ext256k"]
 N_SAMPLES = 40
+
+
+def load_fixture(name):
+    path = os.path.join(GOLDEN, f"fullsize_{name}.npz")
+    assert os.path.exists(path), f"{path} missing: run tests/golden/make_fullsize.py {name}"
+    return dict(np.load(path))
 
 
 def _sample_rows(cfg, lg):
@@ -47,14 +63,21 @@ def _sample_rows(cfg, lg):
     return np.array(sorted(r for r in rows if 0 <= r < N), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["llama3b", "gptoss32k", "long64k", "ext256k"])
-def test_full_size_sampled_parity(name):
+def _run_full(name):
+    """The workload's host-drawn inputs (digest-checked against the
+    fixture) through the debug entry point on the GPU."""
     ensure_lib()
     cfg = workloads.CONFIGS[name]
+    fx = load_fixture(name)
+    for key in ("N", "H", "V", "K", "chunk"):
+        assert int(fx[key]) == getattr(cfg, key), (key, int(fx[key]), getattr(cfg, key))
+    assert float(fx["T"]) == cfg.T
+    inp_cpu = workloads.make_inputs_host(cfg, seed=int(fx["seed"]))
+    assert workloads.input_digest(inp_cpu) == str(fx["digest"]), \
+        "host-drawn inputs differ from the ones the fixture was computed on"
     N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
     dev = torch.device("cuda")
-    inp = workloads.make_inputs(cfg, seed=0, device=dev)
-    h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
+    inp = to_device(inp_cpu, dev)
     gh = torch.empty((N, H), dtype=torch.float32, device=dev)
     gW = torch.empty((V, H), dtype=torch.float32, device=dev)
     ws = kd.alloc_workspace(N, H, V, K, cfg.chunk, device=dev)
@@ -62,52 +85,92 @@ def test_full_size_sampled_parity(name):
     zg = torch.empty((N, K), dtype=torch.float32, device=dev)
     found = torch.full((N, K), -1, dtype=torch.int32, device=dev)
     loss_rows = torch.empty((N,), dtype=torch.float64, device=dev)
-    loss = kd.kd_topk_kl_debug(h, W, idx, lg, T, cfg.chunk, gh, gW, ws, lse=lse, zg=zg,
-                               found_idx=found, loss_rows=loss_rows)
+    loss = kd.kd_topk_kl_debug(inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"], T,
+                               cfg.chunk, gh, gW, ws, lse=lse, zg=zg, found_idx=found,
+                               loss_rows=loss_rows)
     torch.cuda.synchronize()
     del ws
+    return cfg, fx, inp_cpu, inp, loss, dict(gh=gh, gW=gW, lse=lse, zg=zg, found=found,
+                                             loss_rows=loss_rows)
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_full_size_against_oracle(name):
+    cfg, fx, inp_cpu, inp, loss, out = _run_full(name)
+    N, T = cfg.N, cfg.T
+    gh, gW, found, loss_rows = out["gh"], out["gW"], out["found"], out["loss_rows"]
 
     # gathered ids: bit-exact on every row
-    assert torch.equal(found, idx), "a cached id was gathered from the wrong column"
+    assert torch.equal(found, inp["topk_idx"]), "a cached id was gathered from the wrong column"
 
-    # the loss is the mean of the per-token terms (double sum, fp32 result)
+    # the whole-N loss against the oracle's
+    want_loss = float(fx["loss"])
+    assert abs(loss - want_loss) <= LOSS_RTOL * abs(want_loss), (loss, want_loss)
+    # ... and it is the mean of the per-token terms (double sum, fp32 result)
     mean_rows = float(loss_rows.sum().item()) / N
     assert abs(loss - mean_rows) <= 1e-6 * abs(mean_rows), (loss, mean_rows)
-    assert torch.isfinite(gh).all() and torch.isfinite(gW).all()
 
-    # sampled tokens against the oracle
-    rows = _sample_rows(cfg, lg)
-    rt = torch.from_numpy(rows).to(dev)
-    W_cpu = W.cpu()
-    want = oracle.rows_forward(h[rt].cpu(), W_cpu, idx[rt].cpu(), lg[rt].cpu(), T, N_total=N)
-    np.testing.assert_allclose(lse[rt].cpu().numpy(), want["lse"], rtol=0, atol=LSE_ATOL)
+    # every token's normaliser and KL term against the oracle's
+    lse_err = np.abs(out["lse"].cpu().numpy() - fx["lse"].astype(np.float64)).max()
+    assert lse_err <= LSE_ATOL, lse_err
+    np.testing.assert_allclose(loss_rows.cpu().numpy(), fx["loss_rows"].astype(np.float64),
+                               rtol=LOSS_RTOL, atol=1e-5)
+
+    # grad_W rows (each a sum over all N tokens, i.e. over every chunk)
+    assert torch.isfinite(gh).all() and torch.isfinite(gW).all()
+    vrows = torch.from_numpy(fx["vrows"]).to(gW.device)
+    got_rows = gW[vrows].cpu().numpy()
+    want_rows = fx["grad_W_rows"].astype(np.float64)
+    err = rel_l2(got_rows, want_rows)
+    assert err <= GRAD_REL_L2, err
+    # no single row is far off either (rows of non-hit ids are small)
+    row_err = np.linalg.norm(got_rows - want_rows, axis=1) / np.linalg.norm(want_rows, axis=1)
+    assert row_err.max() <= 5 * GRAD_REL_L2, (fx["vrows"][row_err.argmax()], row_err.max())
+
+    # sampled tokens: gathered z and grad_hidden rows against the oracle
+    rows = _sample_rows(cfg, inp_cpu["topk_logit"])
+    want = oracle.rows_forward(inp_cpu["hidden"][rows], inp_cpu["W"], inp_cpu["topk_idx"][rows],
+                               inp_cpu["topk_logit"][rows], T, N_total=N)
+    rt = torch.from_numpy(rows).to(gh.device)
     zscale = max(np.abs(want["zg"]).max(), 1e-6)
-    assert np.abs(zg[rt].cpu().numpy() - want["zg"]).max() <= ZG_RTOL * zscale
-    np.testing.assert_allclose(loss_rows[rt].cpu().numpy(), want["loss_rows"],
-                               rtol=LOSS_RTOL, atol=1e-6)
+    assert np.abs(out["zg"][rt].cpu().numpy() - want["zg"]).max() <= ZG_RTOL * zscale
+    np.testing.assert_allclose(out["lse"][rt].cpu().numpy(), want["lse"], rtol=0, atol=LSE_ATOL)
     err = rel_l2(gh[rt].cpu().numpy(), want["grad_hidden"])
     assert err <= GRAD_REL_L2, err
 
     # grad_W: its vocabulary rows sum to zero, relative to the size of one
     # row-sum's terms (|dZ| summed over v is at most 2/(T N) per token)
+    h = inp["hidden"]
     col = gW.double().sum(dim=0)
     scale = (h.double().abs().sum(dim=0) * (2.0 / (T * N)))
     assert float((col.abs() / scale).max()) <= 1e-3
-
-    # grad_W: <grad_W, W> = <grad_hidden, hidden>
-    a = float((gW.double() * W.double()).sum())
+    # grad_W: <grad_W, W> = <grad_hidden, hidden> (both sum_{n,v} dZ_nv z_nv)
+    a = float((gW.double() * inp["W"].double()).sum())
     b = float((gh.double() * h.double()).sum())
     mag = float((gh.double() * h.double()).abs().sum())
     assert abs(a - b) <= 1e-3 * mag, (a, b, mag)
-    # and the identity is not vacuous: its value is a sizeable part of the scale
     assert abs(b) >= 1e-2 * mag
 
 
-def test_full_vocab_head_grad_W_rows():
-    """256 tokens of the GPT-OSS-like head (H=2880, V=201,088, chunk 2048):
-    every output against the oracle, grad_W on sampled vocabulary rows
-    (teacher-hit rows, the last rows of the ragged last vocab tile, random
-    rows)."""
+def test_llama3b_dense_gradients():
+    """llama3b (8,192 tokens, H=3072, V=128,256, chunk 1024) against the
+    dense float64 oracle run here on the host: all of grad_hidden and
+    grad_W, every lse and gathered z, and the loss."""
+    cfg, fx, inp_cpu, inp, loss, out = _run_full("llama3b")
+    want = oracle.fused_topk_kl(inp_cpu["hidden"], inp_cpu["W"], inp_cpu["topk_idx"],
+                                inp_cpu["topk_logit"], cfg.T)
+    assert abs(want["loss"] - float(fx["loss"])) <= 1e-9 * abs(want["loss"])
+    got = {"loss": loss, "found": out["found"].cpu().numpy(), "lse": out["lse"].cpu().numpy(),
+           "zg": out["zg"].cpu().numpy(), "grad_hidden": out["gh"].cpu().numpy(),
+           "grad_W": out["gW"].cpu().numpy()}
+    assert_parity(got, want, inp_cpu["topk_idx"].numpy())
+
+
+def test_full_vocab_head_single_chunk():
+    """256 tokens of the GPT-OSS-like head (H=2880, V=201,088) in one
+    2048-row chunk: every output against the dense oracle, grad_W on
+    sampled vocabulary rows (teacher-hit rows, the last rows of the ragged
+    last vocab tile, random rows) and in full."""
     ensure_lib()
     base = workloads.CONFIGS["gptoss32k"]
     inp = workloads.make_inputs(base, seed=4, n_rows=256)

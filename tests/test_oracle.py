@@ -48,6 +48,25 @@ def test_rows_forward_matches_full():
         np.testing.assert_allclose(part[key], full[key][rows], rtol=0, atol=1e-13)
 
 
+def test_rows_forward_vocab_rows_add_up_to_full_grad_W():
+    # per-block shares of grad_W rows, summed over disjoint token blocks,
+    # equal the full problem's rows; grad_hidden=False leaves the rest alone
+    h, W, idx, lg = pins.small_case(14, N=23, H=7, V=37, K=5)
+    T = 1.7
+    full = oracle.fused_topk_kl(h, W, idx, lg, T)
+    vrows = np.array([36, 0, int(idx[5, 1]), 11, int(idx[5, 1])])
+    acc = np.zeros((len(vrows), 7))
+    for r0, r1 in ((0, 9), (9, 10), (10, 23)):
+        part = oracle.rows_forward(h[r0:r1], W, idx[r0:r1], lg[r0:r1], T, N_total=23,
+                                   vrows=vrows, grad_hidden=False)
+        assert "grad_hidden" not in part
+        np.testing.assert_allclose(part["lse"], full["lse"][r0:r1], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(part["loss_rows"], full["loss_rows"][r0:r1], rtol=0,
+                                   atol=1e-13)
+        acc += part["grad_W_rows"]
+    np.testing.assert_allclose(acc, full["grad_W"][vrows], rtol=0, atol=1e-14)
+
+
 def test_grad_W_rows_matches_full():
     h, W, idx, lg = pins.small_case(13, N=25, H=6, V=40, K=6)
     full = oracle.fused_topk_kl(h, W, idx, lg, 0.9)

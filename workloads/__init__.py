@@ -33,9 +33,11 @@ values.
 from __future__ import annotations
 
 import dataclasses
+import hashlib
 import math
 from typing import Optional
 
+import numpy as np
 import torch
 
 
@@ -168,6 +170,100 @@ def make_inputs(cfg: Config, seed: int = 0, device="cpu",
     idx = distinct_ids(gen, N, cfg.K, cfg.V, device=device)
     logit = teacher_logits(cfg, gen, N, device=device)
     return {"hidden": hidden, "W": W, "topk_idx": idx, "topk_logit": logit}
+
+
+def make_inputs_host(cfg: Config, seed: int = 0,
+                     n_rows: Optional[int] = None) -> dict:
+    """Draw (hidden, W, topk_idx, topk_logit) for ``cfg`` on the host with
+    numpy's PCG64 generator.
+
+    The recipe is that of ``make_inputs`` (same distributions, same stream
+    order: hidden, W, ids, teacher logits, spikes), but every value comes
+    from numpy's bit generator and IEEE-exact arithmetic (multiplies,
+    divides, square roots, fp32 -> bf16 rounding to nearest even), so the
+    same seed gives the same bytes on any host with this numpy.  Values
+    that a committed script computed from these inputs on one machine can
+    therefore be compared with a GPU run on another (``input_digest``
+    checks that the bytes agree).
+
+    Returns CPU tensors with the dtypes and layouts of ``make_inputs``.
+    """
+    N = cfg.N if n_rows is None else n_rows
+    H, V, K = cfg.H, cfg.V, cfg.K
+    rng = np.random.Generator(np.random.PCG64(seed))
+    # normal draws in float64 (numpy's fast path), rounded to fp32, in row
+    # blocks to bound the temporaries; consecutive blocks continue the stream
+    hidden = np.empty((N, H), dtype=np.float32)
+    for r0 in range(0, N, _HOST_BLOCK):
+        blk = rng.standard_normal((min(N, r0 + _HOST_BLOCK) - r0, H))
+        if cfg.hidden_rms_norm:
+            # each row divided by its RMS (computed from the fp32 values)
+            blk = blk.astype(np.float32).astype(np.float64)
+            blk = blk / np.sqrt((blk * blk).sum(axis=1, keepdims=True) / H)
+        hidden[r0:r0 + blk.shape[0]] = blk
+    hidden_t = torch.from_numpy(hidden).to(torch.bfloat16)
+    del hidden
+    W = np.empty((V, H), dtype=np.float32)
+    for r0 in range(0, V, _HOST_BLOCK):
+        blk = rng.standard_normal((min(V, r0 + _HOST_BLOCK) - r0, H)).astype(np.float32)
+        W[r0:r0 + blk.shape[0]] = blk * np.float32(cfg.w_std)
+    W_t = torch.from_numpy(W).to(torch.bfloat16)
+    del W
+    idx = _distinct_ids_host(rng, N, K, V)
+    if cfg.teacher == "exp_gaps":
+        gaps = rng.exponential(scale=cfg.gap_scale, size=(N, K - 1))
+        lg = np.empty((N, K), dtype=np.float64)
+        lg[:, 0] = 10.0
+        lg[:, 1:] = 10.0 - np.cumsum(gaps, axis=1)
+    elif cfg.teacher == "zipf":
+        # scalar libm logs of 1..K (no vectorised math in the recipe)
+        row = np.array([10.0 - math.log(k) for k in range(1, K + 1)], dtype=np.float64)
+        lg = np.repeat(row[None, :], N, axis=0)
+    else:
+        raise ValueError(cfg.teacher)
+    if cfg.spike_frac > 0:
+        spike = rng.random(N) < cfg.spike_frac
+        lg[:, 0] += np.where(spike, cfg.spike, 0.0)
+    return {"hidden": hidden_t, "W": W_t, "topk_idx": torch.from_numpy(idx),
+            "topk_logit": torch.from_numpy(lg.astype(np.float32))}
+
+
+_HOST_BLOCK = 8192
+
+
+def _distinct_ids_host(rng: np.random.Generator, n: int, k: int, v: int) -> np.ndarray:
+    """[n, k] int32 ids, distinct within each row, uniform over [0, v):
+    uniform draws, then the later copy of every repeated id in a row is
+    redrawn until no row holds a repeat (rows left unsorted)."""
+    if k > v:
+        raise ValueError("cannot draw k > v distinct ids")
+    if k == v:
+        return rng.permuted(np.tile(np.arange(v, dtype=np.int32), (n, 1)), axis=1)
+    ids = rng.integers(0, v, size=(n, k), dtype=np.int64)
+    for _ in range(10000):
+        order = np.argsort(ids, axis=1, kind="stable")
+        srt = np.take_along_axis(ids, order, axis=1)
+        dup_sorted = np.zeros(srt.shape, dtype=bool)
+        dup_sorted[:, 1:] = srt[:, 1:] == srt[:, :-1]
+        if not dup_sorted.any():
+            return ids.astype(np.int32)
+        dup = np.zeros_like(dup_sorted)
+        np.put_along_axis(dup, order, dup_sorted, axis=1)
+        ids[dup] = rng.integers(0, v, size=int(dup.sum()), dtype=np.int64)
+    raise RuntimeError("distinct id redraw did not converge")
+
+
+def input_digest(inp: dict) -> str:
+    """SHA-256 of the raw bytes of (hidden, W, topk_idx, topk_logit), in
+    that order: equal digests mean bit-identical inputs."""
+    h = hashlib.sha256()
+    for key in ("hidden", "W", "topk_idx", "topk_logit"):
+        t = inp[key].detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        h.update(key.encode())
+        h.update(t.numpy().tobytes())
+    return h.hexdigest()
 
 
 def bytes_of_inputs(cfg: Config) -> dict:
