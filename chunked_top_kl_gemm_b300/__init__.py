@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
     L.kd_topk_kl_fwd_bwd_flags.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
                                             ctypes.c_uint, vp, vp, vp, vp, sz, vp]
     L.kd_topk_kl_fwd_bwd_flags.restype = i32
+    L.kd_topk_kl_fwd_bwd_sharded.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
+                                              ctypes.c_uint, i64, vp, vp, vp, vp, sz, vp]
+    L.kd_topk_kl_fwd_bwd_sharded.restype = i32
     L.kd_topk_kl_fwd_bwd_async.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, f32, i32,
                                             ctypes.c_uint, vp, vp, vp, vp, vp, sz, vp]
     L.kd_topk_kl_fwd_bwd_async.restype = i32
@@ -280,6 +283,26 @@ def kd_topk_kl_fwd_bwd_flags(hidden, W, topk_idx, topk_logit, token_mask, T: flo
             _ptr(grad_W), _ptr(workspace), workspace.numel() * workspace.element_size(),
             _stream_handle(stream))
     _check(st, "kd_topk_kl_fwd_bwd_flags")
+    return float(loss.value)
+
+
+def kd_topk_kl_fwd_bwd_sharded(hidden, W, topk_idx, topk_logit, token_mask, T: float,
+                               chunk: int, flags: int, n_norm: int, grad_hidden, grad_W,
+                               workspace, stream=None) -> float:
+    """One shard of a batch whose mean runs over ``n_norm`` tokens: the
+    returned loss and the gradients are normalised by the whole batch, so
+    shards' losses and grad_W add up to the batch's (``KD_FLAG_ACCUMULATE``
+    adds into grad_W on one device)."""
+    N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    token_mask = _check_mask(token_mask, N)
+    loss = ctypes.c_float(0.0)
+    with _on_device(hidden):
+        st = lib().kd_topk_kl_fwd_bwd_sharded(
+            _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
+            float(T), int(chunk), int(flags), int(n_norm), ctypes.addressof(loss),
+            _ptr(grad_hidden), _ptr(grad_W), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "kd_topk_kl_fwd_bwd_sharded")
     return float(loss.value)
 
 

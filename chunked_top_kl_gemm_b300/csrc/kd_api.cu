@@ -273,11 +273,15 @@ kd_status validate(const void* hidden, const void* W, const int32_t* idx, const 
 // forward GEMM and forms dZ from them instead of recomputing the GEMM.
 // async (loss_dev and status_dev device words): nothing waits for the
 // stream; the last kernel writes the loss and the status code.
+// n_norm > 0 (a shard of a larger batch): the gradients are scaled by
+// 1/(T n_norm) and the returned loss is the shard's sum of per-token terms
+// divided by n_norm, so that shards' results add up to the whole batch's.
 kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const float* logit,
                    long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
                    float* gW, void* ws, size_t ws_bytes, cudaStream_t s,
                    const kd_debug_opts* opts, const uint8_t* mask, unsigned flags,
-                   float* loss_dev = nullptr, int32_t* status_dev = nullptr) {
+                   float* loss_dev = nullptr, int32_t* status_dev = nullptr,
+                   double n_norm = 0.0) {
   const bool async = loss_dev != nullptr;
   const int accumulate = (flags & KD_FLAG_ACCUMULATE) ? 1 : 0;
   const bool store_z = (flags & KD_FLAG_STORE_LOGITS) != 0;
@@ -342,16 +346,19 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     return KD_ERR_CUDA;
   }
 
+  const bool sharded = n_norm > 0.0;
   const float scale2 = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
-  const float alpha = static_cast<float>(1.0 / (static_cast<double>(T) * static_cast<double>(N)));
+  const float alpha = static_cast<float>(
+      1.0 / (static_cast<double>(T) * (sharded ? n_norm : static_cast<double>(N))));
 
   KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
   // masked calls: n_valid and the gradient scale 1/(T n_valid) on the device
+  // (a shard's scale is the host's 1/(T n_norm) instead)
   const float* alpha_dev = nullptr;
   if (mask) {
     ProfScope ps_(PK_MASK, s);
     KD_CUDA(kd::launch_mask_count(mask, N, T, dst, s));
-    alpha_dev = &dst->alpha;
+    if (!sharded) alpha_dev = &dst->alpha;
   }
   { ProfScope ps_(PK_PREP, s); KD_CUDA(kd::launch_prep_topk(idx, logit, N, K, V, T, sid, sp, perm, ent, psum, dst, s)); }
 
@@ -449,8 +456,8 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   prof_collect();
   if (hs.err & kd::DEV_ERR_TIMEOUT) return KD_ERR_TIMEOUT;
   if (hs.err & kd::DEV_ERR_INDEX) return KD_ERR_INDEX;
-  const long long n_mean = mask ? hs.n_valid : N;
-  *loss = n_mean > 0 ? static_cast<float>(hs.loss_sum / static_cast<double>(n_mean)) : 0.f;
+  const double n_mean = sharded ? n_norm : static_cast<double>(mask ? hs.n_valid : N);
+  *loss = n_mean > 0 ? static_cast<float>(hs.loss_sum / n_mean) : 0.f;
   return KD_OK;
 }
 
@@ -460,9 +467,9 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
 kd_status run(const void* hidden, const void* W, const int32_t* idx, const float* logit,
               long long N, int H, int V, int K, float T, int chunk, float* loss, float* gh,
               float* gW, void* ws, size_t ws_bytes, cudaStream_t s, const kd_debug_opts* opts,
-              const uint8_t* mask = nullptr, unsigned flags = 0) {
+              const uint8_t* mask = nullptr, unsigned flags = 0, double n_norm = 0.0) {
   const kd_status st = run_impl(hidden, W, idx, logit, N, H, V, K, T, chunk, loss, gh, gW, ws,
-                                ws_bytes, s, opts, mask, flags);
+                                ws_bytes, s, opts, mask, flags, nullptr, nullptr, n_norm);
   if (st == KD_ERR_CUDA) {
     cudaStreamSynchronize(s);
     cudaGetLastError();
@@ -514,6 +521,18 @@ kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int3
   return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
              workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, token_mask,
              flags);
+}
+
+kd_status kd_topk_kl_fwd_bwd_sharded(const void* hidden, const void* W, const int32_t* topk_idx,
+                                     const float* topk_logit, const uint8_t* token_mask,
+                                     int64_t N, int H, int V, int K, float T, int chunk,
+                                     unsigned flags, int64_t n_norm, float* loss,
+                                     float* grad_hidden, float* grad_W, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (n_norm < 1) return KD_ERR_INVALID_ARG;
+  return run(hidden, W, topk_idx, topk_logit, N, H, V, K, T, chunk, loss, grad_hidden, grad_W,
+             workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, token_mask,
+             flags, static_cast<double>(n_norm));
 }
 
 kd_status kd_topk_kl_fwd_bwd_async(const void* hidden, const void* W, const int32_t* topk_idx,

@@ -186,6 +186,37 @@ kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int3
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * One shard of a batch whose loss is the mean over n_norm tokens.
+ *
+ * The pages' headline run distils GPT-OSS 20B at 32K context on one node
+ * instead of four (glonce.com, body and "Key facts"); a data-parallel
+ * trainer splits a batch's tokens across devices, and a single-device
+ * trainer may split them into micro-batches.  Both need each shard's loss
+ * and gradients normalised by the whole batch's token count, so that the
+ * shards' results add up:
+ *
+ *   loss (out)   (1/n_norm) sum over this shard's (valid) tokens of the
+ *                per-token KL terms; the batch loss is the sum over shards
+ *   grad_hidden  this shard's rows, scaled by 1/(T n_norm): final as they are
+ *   grad_W       this shard's share, scaled by 1/(T n_norm); the batch's
+ *                grad_W is the sum of the shards' (add them with
+ *                KD_FLAG_ACCUMULATE on one device, or an all-reduce across
+ *                devices)
+ *   n_norm       >= 1: the number of tokens the batch's mean runs over (with
+ *                masks, the batch's valid tokens); KD_ERR_INVALID_ARG otherwise
+ *
+ * Everything else as for kd_topk_kl_fwd_bwd_flags (N, hidden, topk_* and
+ * token_mask describe the shard).  With n_norm = N (or N_v for a masked
+ * call) the results equal kd_topk_kl_fwd_bwd_flags's.
+ */
+kd_status kd_topk_kl_fwd_bwd_sharded(const void* hidden, const void* W, const int32_t* topk_idx,
+                                     const float* topk_logit, const uint8_t* token_mask,
+                                     int64_t N, int H, int V, int K, float T, int chunk,
+                                     unsigned flags, int64_t n_norm, float* loss,
+                                     float* grad_hidden, float* grad_W, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * Asynchronous form of kd_topk_kl_fwd_bwd_flags, for a training step that
  * keeps the host out of the loop or captures the step in a CUDA graph.  It
  * enqueues the whole path on `stream` and returns without synchronising:

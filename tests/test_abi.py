@@ -111,3 +111,22 @@ def test_async_entry_checks_arguments_before_enqueueing(L):
     ptrs[4] += 8
     assert _call_async(L, ptrs) == 2
     assert _call_async(L, GOOD, N=0) == 1
+
+
+def test_sharded_entry_checks_its_normaliser_and_arguments(L):
+    h, w, i, l, gh, gw = GOOD
+    out = ctypes.c_float(0)
+
+    def call(n_norm, hidden=h, N=16):
+        return L.kd_topk_kl_fwd_bwd_sharded(hidden, w, i, l, None, N, 64, 128, 4, 1.0, 128, 0,
+                                            n_norm, ctypes.addressof(out), gh, gw, 0x90000,
+                                            1 << 30, None)
+    assert call(0) == 1 and call(-5) == 1
+    assert call(32, hidden=None) == 1
+    assert call(32, N=0) == 1
+
+
+def test_flags_outside_the_defined_set_are_rejected(L):
+    for bad in (8, 16, 1 << 31):
+        assert L.kd_topk_kl_workspace_size_flags(16, 64, 128, 4, 128, bad) == 0
+    assert L.kd_topk_kl_workspace_size_flags(16, 64, 128, 4, 128, kd.KD_FLAG_MIN_SCRATCH) > 0
