@@ -309,12 +309,15 @@ def run_gpu(args):
     chunk = args.chunk or cfg.chunk
     N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
 
-    torch.cuda.reset_peak_memory_stats(dev)
     mem0 = torch.cuda.memory_allocated(dev)
     torch.cuda.synchronize(dev)
     nvml0 = nvml_used_bytes(dev)
     inp = workloads.make_inputs(cfg, seed=rank, device=dev)
     h, W, idx, lg = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
+    # the peak counts the resident inputs, outputs, workspace and whatever the
+    # calls allocate, not the temporaries of drawing the inputs on the device
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
     gh = torch.empty((N, H), dtype=torch.float32, device=dev)
     gW = torch.empty((V, H), dtype=torch.float32, device=dev)
     flags = (kd.KD_FLAG_STORE_LOGITS if args.store_logits else 0) | \
@@ -535,18 +538,24 @@ def run_sweep(args):
         torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
         mem0 = torch.cuda.memory_allocated(dev)
-        torch.cuda.reset_peak_memory_stats(dev)
         inp = workloads.make_inputs(cfg, seed=0, device=dev)
+        torch.cuda.synchronize(dev)
+        torch.cuda.reset_peak_memory_stats(dev)     # not the input draw's temporaries
         gh = torch.empty((N, H), dtype=torch.float32, device=dev)
         gW = torch.empty((V, H), dtype=torch.float32, device=dev)
-        ws = kd.alloc_workspace(N, H, V, K, chunk, device=dev)
-        args_ = (inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"], T, chunk, gh, gW, ws)
-        loss = kd.kd_topk_kl_fwd_bwd_ex(*args_)
+        flags = kd.KD_FLAG_MIN_SCRATCH if args.min_scratch else 0
+        ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, flags),
+                         dtype=torch.uint8, device=dev)
+        h_, W_, i_, l_ = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
+
+        def call():
+            return kd.kd_topk_kl_fwd_bwd_flags(h_, W_, i_, l_, None, T, chunk, flags, gh, gW, ws)
+        loss = call()
         torch.cuda.synchronize(dev)
         peak = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
         # time one more warm call, then enough steps for ~1.5 s of samples
         w0 = time.perf_counter()
-        kd.kd_topk_kl_fwd_bwd_ex(*args_)
+        call()
         steps = max(3, min(200, int(1.5 / max(time.perf_counter() - w0, 1e-4)) + 1))
         clocks = ClockSampler(_gpu_id(0))
         clocks.start()
@@ -555,14 +564,16 @@ def run_sweep(args):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(steps):
-            loss = kd.kd_topk_kl_fwd_bwd_ex(*args_)
+            loss = call()
         e1.record()
         torch.cuda.synchronize(dev)
         clk = clocks.stop()
         t = e0.elapsed_time(e1) / 1e3 / steps
         tflops = cfg.flops / t / 1e12
         print(json.dumps({
-            "sweep": "memory_and_throughput", "workload": cfg.name, "N": N, "H": H, "V": V,
+            "sweep": "memory_and_throughput", "workload": cfg.name,
+            "grad_W_depth": "one chunk (minimal scratch)" if args.min_scratch else "two chunks",
+            "N": N, "H": H, "V": V,
             "K": K, "T": T, "chunk": chunk, "steps": steps, "tokens_per_s": N / t,
             "ms_per_step": t * 1e3, "tflops": tflops,
             "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
@@ -572,7 +583,7 @@ def run_sweep(args):
             "workspace_gib": ws.numel() / 2**30,
             "dense_fp32_logits_gib": 4 * N * V / 2**30, "loss": loss,
             "clocks": clk, "cpu_baseline": oracle_rate.get(name)}), flush=True)
-        del inp, gh, gW, ws, args_
+        del inp, gh, gW, ws, h_, W_, i_, l_
 
 
 # ------------------------------------------------------------------ cache builder

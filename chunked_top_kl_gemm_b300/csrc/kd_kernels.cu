@@ -300,15 +300,18 @@ cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N
 }
 
 // ------------------------------------------------------------------ lse + loss fold
-// One block per 32 chunk rows (32 warps).  Lane l of every warp owns row
-// r0 + l; warp w combines the (max, sum) partials of vocab tiles w, w+32, ...
-// (log2 units, loads coalesced over the rows, four in flight per lane) in
-// fp32 relative to its running max, then warp 0 merges the 32 results in
-// double into lse2 = log2 sum_v 2^(z_v log2e / T).  Warp w then folds row
-// r0 + w's KL term  sum_k p_k (log p_k - z_k/T + lse),  lse = lse2 ln 2,
-// with the lanes striding over the K cached entries.
-constexpr int LSE_ROWS = 32;
+// One block per 8 chunk rows (32 warps).  Lane l of warp w takes row
+// r0 + (l & 7) and the vocab tiles t = p + 4 (w + 32 i), p = l >> 3: it
+// combines their (max, sum) partials (log2 units) in fp32 relative to its
+// running max, a warp load covering 4 tiles x 8 consecutive rows.  Warp
+// w < 8 then merges row r0 + w's 128 partial pairs in double into
+// lse2 = log2 sum_v 2^(z_v log2e / T), and folds the row's KL term
+// sum_k p_k (log p_k - z_k/T + lse),  lse = lse2 ln 2,  with the lanes
+// striding over the K cached entries.
+constexpr int LSE_ROWS = 8;
+constexpr int LSE_PHASES = 4;     // lanes per row in a warp
 constexpr int LSE_WARPS = 32;
+constexpr int LSE_SLOTS = LSE_WARPS * LSE_PHASES;   // partial pairs per row
 
 __device__ __forceinline__ void lse_fold(float& M, float& S, float2 v) {
   const float m_new = fmaxf(M, v.x);
@@ -322,56 +325,65 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
     const double* __restrict__ ent, const double* __restrict__ psum, int K, double invT,
     const uint8_t* __restrict__ mask, float* __restrict__ lse2_out,
     double* __restrict__ loss_rows, float* __restrict__ dbg_lse, float* __restrict__ dbg_zg) {
-  __shared__ float sM[LSE_WARPS][LSE_ROWS + 1];
-  __shared__ float sS[LSE_WARPS][LSE_ROWS + 1];
-  __shared__ double sLse[LSE_ROWS];
+  __shared__ float sM[LSE_ROWS][LSE_SLOTS + 1];
+  __shared__ float sS[LSE_ROWS][LSE_SLOTS + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = blockIdx.x * LSE_ROWS;
-  const int r = r0 + lane;
+  const int rr = lane & (LSE_ROWS - 1), ph = lane / LSE_ROWS;
+  const int r = r0 + rr;
   float M = -CUDART_INF_F, S = 0.f;
   if (r < rows_valid) {
     const float2* col = part + r;
-    int t = warp;
-    for (; t + 3 * LSE_WARPS < n_tiles; t += 4 * LSE_WARPS) {
-      float2 v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = col[static_cast<long long>(t + i * LSE_WARPS) * c_alloc];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) lse_fold(M, S, v[i]);
+    constexpr int STEP = LSE_PHASES * LSE_WARPS;
+    int t = ph + LSE_PHASES * warp;
+    for (; t + STEP < n_tiles; t += 2 * STEP) {
+      const float2 a = col[static_cast<long long>(t) * c_alloc];
+      const float2 b = col[static_cast<long long>(t + STEP) * c_alloc];
+      lse_fold(M, S, a);
+      lse_fold(M, S, b);
     }
-    for (; t < n_tiles; t += LSE_WARPS) lse_fold(M, S, col[static_cast<long long>(t) * c_alloc]);
+    if (t < n_tiles) lse_fold(M, S, col[static_cast<long long>(t) * c_alloc]);
   }
-  sM[warp][lane] = M;
-  sS[warp][lane] = S;
+  const int slot = warp * LSE_PHASES + ph;
+  sM[rr][slot] = M;
+  sS[rr][slot] = S;
   __syncthreads();
-  if (warp == 0) {
-    float Mr = -CUDART_INF_F;
-    for (int w = 0; w < LSE_WARPS; ++w) Mr = fmaxf(Mr, sM[w][lane]);
-    double Sr = 0.0;
-    for (int w = 0; w < LSE_WARPS; ++w)
-      if (sS[w][lane] > 0.f)
-        Sr += static_cast<double>(sS[w][lane]) * static_cast<double>(exp2f(sM[w][lane] - Mr));
-    const double lse2 = static_cast<double>(Mr) + log2(Sr);
-    sLse[lane] = lse2 * 0.69314718055994530942;  // ln 2
-    if (r < rows_valid) lse2_out[r] = static_cast<float>(lse2);
-  }
-  __syncthreads();
+  if (warp >= LSE_ROWS) return;
   const int row = r0 + warp;
-  if (row < rows_valid) {
-    const long long g = static_cast<long long>(grow0) + row;
-    double dot = 0.0;
-    for (int j = lane; j < K; j += 32) {
-      const float z = zg[static_cast<long long>(row) * K + j];
-      dot += static_cast<double>(sp[g * K + j]) * static_cast<double>(z);
-      if (dbg_zg) dbg_zg[g * K + perm[g * K + j]] = z;
-    }
+  if (row >= rows_valid) return;                 // warp-uniform
+  // merge the row's partial pairs: max over the lanes, then the sum in double
+  float m4[LSE_SLOTS / 32], s4[LSE_SLOTS / 32];
+  float Mr = -CUDART_INF_F;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if (lane == 0) {
-      const bool live = !mask || mask[g] != 0;
-      loss_rows[g] = live ? ent[g] + sLse[warp] * psum[g] - dot * invT : 0.0;
-      if (dbg_lse) dbg_lse[g] = static_cast<float>(sLse[warp]);
-    }
+  for (int i = 0; i < LSE_SLOTS / 32; ++i) {
+    m4[i] = sM[warp][lane + 32 * i];
+    s4[i] = sS[warp][lane + 32 * i];
+    Mr = fmaxf(Mr, m4[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, o));
+  double Sr = 0.0;
+#pragma unroll
+  for (int i = 0; i < LSE_SLOTS / 32; ++i)
+    if (s4[i] > 0.f) Sr += static_cast<double>(s4[i]) * static_cast<double>(exp2f(m4[i] - Mr));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Sr += __shfl_xor_sync(0xffffffffu, Sr, o);
+  const double lse2 = static_cast<double>(Mr) + log2(Sr);
+  const double lse = lse2 * 0.69314718055994530942;  // ln 2
+  const long long g = static_cast<long long>(grow0) + row;
+  double dot = 0.0;
+  for (int j = lane; j < K; j += 32) {
+    const float z = zg[static_cast<long long>(row) * K + j];
+    dot += static_cast<double>(sp[g * K + j]) * static_cast<double>(z);
+    if (dbg_zg) dbg_zg[g * K + perm[g * K + j]] = z;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  if (lane == 0) {
+    lse2_out[row] = static_cast<float>(lse2);
+    const bool live = !mask || mask[g] != 0;
+    loss_rows[g] = live ? ent[g] + lse * psum[g] - dot * invT : 0.0;
+    if (dbg_lse) dbg_lse[g] = static_cast<float>(lse);
   }
 }
 
