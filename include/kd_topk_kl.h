@@ -27,8 +27,9 @@
  *
  * Arithmetic.  hidden and W are bf16; the GEMMs run on tcgen05 tensor cores
  * with fp32 accumulation; the per-token loss terms and their sum are
- * accumulated in double; dZ is held per chunk as bf16 scratch (chunk x V);
- * grad_W is accumulated over chunks in fp32 in device memory.
+ * accumulated in double; dZ is held as bf16 scratch for two consecutive
+ * chunks (2 x chunk x V; one chunk with KD_FLAG_MIN_SCRATCH); grad_W is
+ * accumulated over those chunk pairs in fp32 in device memory.
  *
  * Pointers.  Unless stated otherwise every array argument is a DEVICE
  * pointer (cudaMalloc / cudaMallocAsync / managed memory on the current
@@ -90,7 +91,8 @@ typedef enum kd_status {
  *   T           temperature, finite and > 0
  *   chunk       token rows per chunk (>= 1); rounded up to a multiple of 128
  *               and capped at N rounded up likewise.  Scratch grows as
- *               chunk x V x 2 bytes.
+ *               2 x chunk x V x 2 bytes (the bf16 dZ of two chunks; one
+ *               chunk's when N fits in one chunk).
  *   loss        HOST float*: the mean over the N tokens
  *   grad_hidden fp32 [N, H] (device), overwritten
  *   grad_W      fp32 [V, H] (device), overwritten

@@ -27,7 +27,7 @@ def _ws(N, H, V, K, chunk, flags=0):
                        dtype=torch.uint8, device="cuda")
 
 
-def _run_shards(inp, mask, n_norm):
+def _run_shards(inp, mask, n_norm, extra=0):
     N, H = inp["hidden"].shape
     V, K = inp["W"].shape[0], inp["topk_idx"].shape[1]
     # the first shard overwrites grad_W, the others add to it; KD_FLAG_ACCUMULATE
@@ -36,7 +36,7 @@ def _run_shards(inp, mask, n_norm):
     gW = torch.full((V, H), float("nan"), dtype=torch.float32, device="cuda")
     total = 0.0
     for i, (r0, r1) in enumerate(SHARDS):
-        flags = kd.KD_FLAG_ACCUMULATE if i > 0 else 0
+        flags = (kd.KD_FLAG_ACCUMULATE if i > 0 else 0) | extra
         ws = _ws(r1 - r0, H, V, K, CFG.chunk, flags)
         m = None if mask is None else mask[r0:r1]
         total += kd.kd_topk_kl_fwd_bwd_sharded(
@@ -46,14 +46,14 @@ def _run_shards(inp, mask, n_norm):
     return total, gh.cpu().numpy(), gW.cpu().numpy()
 
 
-def _run_whole(inp, mask):
+def _run_whole(inp, mask, extra=0):
     N, H = inp["hidden"].shape
     V, K = inp["W"].shape[0], inp["topk_idx"].shape[1]
     gh = torch.empty((N, H), dtype=torch.float32, device="cuda")
     gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
     loss = kd.kd_topk_kl_fwd_bwd_flags(inp["hidden"], inp["W"], inp["topk_idx"],
-                                       inp["topk_logit"], mask, CFG.T, CFG.chunk, 0, gh, gW,
-                                       _ws(N, H, V, K, CFG.chunk))
+                                       inp["topk_logit"], mask, CFG.T, CFG.chunk, extra, gh, gW,
+                                       _ws(N, H, V, K, CFG.chunk, extra))
     torch.cuda.synchronize()
     return loss, gh.cpu().numpy(), gW.cpu().numpy()
 
@@ -108,3 +108,17 @@ def test_normaliser_below_one_is_rejected():
                                       inp["topk_logit"], None, CFG.T, CFG.chunk, 0, 0, gh, gW,
                                       _ws(N, H, V, K, CFG.chunk))
     assert ei.value.name == "KD_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("extra", ["store_logits", "min_scratch"])
+def test_shards_add_up_with_other_flags(extra):
+    # the stored-logits backward and the per-chunk grad_W form take the same
+    # normaliser
+    ensure_lib()
+    flag = {"store_logits": kd.KD_FLAG_STORE_LOGITS, "min_scratch": kd.KD_FLAG_MIN_SCRATCH}[extra]
+    inp = to_device(workloads.make_inputs(CFG, seed=20))
+    loss, gh, gW = _run_shards(inp, None, CFG.N, extra=flag)
+    ref_loss, ref_gh, ref_gW = _run_whole(inp, None, extra=flag)
+    assert abs(loss - ref_loss) <= 1e-6 * abs(ref_loss), (loss, ref_loss)
+    assert rel_l2(gh, ref_gh) <= 1e-6
+    assert rel_l2(gW, ref_gW) <= 1e-5
