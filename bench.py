@@ -32,7 +32,25 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s fused top-K KL fwd+bwd (N×H×V), % bf16 tensor peak, peak GiB"
-GEMM_KINDS = ("gemm_fwd_lse_gather", "gemm_bwd_dz", "gemm_grad_hidden", "gemm_grad_W")
+GEMM_KINDS = ("gemm_fwd_lse_gather", "gemm_bwd_dz", "gemm_dz_and_next_fwd", "gemm_grad_hidden",
+              "gemm_grad_W")
+
+
+def gemm_flops_per_step(kind: str, N: int, H: int, V: int, chunk: int, store_logits: bool) -> float:
+    """Flops one step spends in the GEMM launches of a profiler kind: 2 H V
+    per token row multiplied.  The forward of the first chunk runs alone and
+    every later chunk's forward shares a launch with the previous chunk's
+    recompute; the last chunk's recompute runs alone.  With stored logits
+    every chunk's forward runs alone and nothing is recomputed."""
+    c = min(-(-chunk // 128) * 128, -(-N // 128) * 128)
+    n = -(-N // c)
+    first = min(c, N)
+    last = N - (n - 1) * c
+    rows = {"gemm_fwd_lse_gather": N if store_logits else first,
+            "gemm_bwd_dz": 0 if store_logits else last,
+            "gemm_dz_and_next_fwd": 0 if store_logits else (N - last) + (N - first),
+            "gemm_grad_hidden": N, "gemm_grad_W": N}[kind]
+    return 2.0 * rows * H * V
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -437,8 +455,8 @@ def run_gpu(args):
     gemm = {k: prof[k] for k in GEMM_KINDS if k in prof and prof[k][1] > 0}
     dom = max(gemm, key=lambda k: gemm[k][0])
     dom_ms, dom_launches = gemm[dom]
-    # the dominant GEMM's launches together do 2NHV flop per step
-    flops_per_launch = 2.0 * N * H * V / (dom_launches / prof_steps)
+    dom_flops = gemm_flops_per_step(dom, N, H, V, chunk, args.store_logits)
+    flops_per_launch = dom_flops / (dom_launches / prof_steps)
     achieved = flops_per_launch / (dom_ms / dom_launches / 1e3) / 1e12
     peak_sust = float(peaks["bf16_tflops_sustained"])
     traffic = stored_traffic(dom, cfg.name)

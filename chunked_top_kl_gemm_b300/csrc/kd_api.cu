@@ -37,12 +37,12 @@ constexpr unsigned kAllFlags = KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS | KD_FL
 // synchronisation the elapsed times are added to per-kind totals.
 enum ProfKind { PK_PREP = 0, PK_FWD, PK_LSE, PK_DZ, PK_GRAD_H, PK_SPLIT_RED, PK_GRAD_W,
                 PK_FINAL, PK_TRANSPOSE, PK_MASK, PK_DZ_EW, PK_CACHE_GEMM, PK_CACHE_SELECT,
-                PK_COUNT };
+                PK_DZ_FWD, PK_COUNT };
 const char* const kProfNames[PK_COUNT] = {"prep_topk", "gemm_fwd_lse_gather", "lse_loss_fold",
                                           "gemm_bwd_dz", "gemm_grad_hidden", "split_reduce",
                                           "gemm_grad_W", "loss_final", "transpose_chunk",
                                           "mask_count", "dz_from_logits", "cache_gemm_logits",
-                                          "cache_topk_select"};
+                                          "cache_topk_select", "gemm_dz_and_next_fwd"};
 
 struct Profiler {
   std::mutex mu;
@@ -382,16 +382,23 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     e.sid = sid; e.sp = sp; e.perm = perm; e.part = part; e.zg = zg; e.lse2 = lse2;
     e.dbg_found = dbg_found;
     e.mask = mask;
-    if (store_z) {
-      ProfScope ps_(PK_FWD, s);
-      KD_CUDA(kd::launch_gemm(kd::GV_FWDZ, tm_hid_k, tm_w_k, tm_z_st, g, e, s));
-    } else {
-      ProfScope ps_(PK_FWD, s);
-      KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e, s));
+    // chunk j's forward: its own launch for the first chunk (and for every
+    // chunk when the logits are stored); otherwise it ran inside the previous
+    // chunk's recompute launch
+    auto lse_of = [&](int r0, int rows) {
+      return kd::launch_lse_loss(part, p.vt, p.chunk, rows, r0, zg, sp, perm, ent, psum, K, T,
+                                 mask, lse2, loss_rows, dbg_lse, dbg_zg, s);
+    };
+    if (store_z || j == 0) {
+      if (store_z) {
+        ProfScope ps_(PK_FWD, s);
+        KD_CUDA(kd::launch_gemm(kd::GV_FWDZ, tm_hid_k, tm_w_k, tm_z_st, g, e, s));
+      } else {
+        ProfScope ps_(PK_FWD, s);
+        KD_CUDA(kd::launch_gemm(kd::GV_FWD, tm_hid_k, tm_w_k, tm_dz_st, g, e, s));
+      }
+      { ProfScope ps_(PK_LSE, s); KD_CUDA(lse_of(row0, cj)); }
     }
-
-    { ProfScope ps_(PK_LSE, s); KD_CUDA(kd::launch_lse_loss(part, p.vt, p.chunk, cj, row0, zg, sp, perm, ent, psum, K, T, mask, lse2,
-                                loss_rows, dbg_lse, dbg_zg, s)); }
 
     g.inject_timeout = (j == 0 && inject == 2);
     if (store_z) {
@@ -400,6 +407,21 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
       ProfScope ps_(PK_DZ_EW, s);
       KD_CUDA(kd::launch_dz_from_z(zbuf, V, cj, cover, lse2, scale2, mask, row0, sid, sp, K,
                                    dz_slot, s));
+    } else if (j + 1 < p.n_chunks) {
+      // the recompute of chunk j (tiles below m_split) and the forward of
+      // chunk j+1 (the tiles after) in one launch: W is streamed once for both
+      const int row1 = row0 + p.chunk;
+      const int cj1 = static_cast<int>(std::min<long long>(p.chunk, N - row1));
+      const int tm = kd::gemm_tile_m(kd::GV_DZFWD);
+      g.m_split = mt;
+      g.m_tiles = mt + static_cast<int>(cdiv(cj1, tm));
+      g.a_row0_b = row1 - mt * tm;                   // tile m_split starts at row1
+      e.out_row0 = slot_row0;                        // dZ rows of chunk j's slot
+      e.grow0_b = row1; e.rows_valid_b = cj1;
+      { ProfScope ps_(PK_DZ_FWD, s);
+        KD_CUDA(kd::launch_gemm(kd::GV_DZFWD, tm_hid_k, tm_w_k, tm_dz_st, g, e, s)); }
+      // chunk j+1's logsumexp and loss terms (chunk j's lse2 is consumed)
+      { ProfScope ps_(PK_LSE, s); KD_CUDA(lse_of(row1, cj1)); }
     } else {
       e.out_row0 = slot_row0;                        // dZ rows of this chunk's slot
       ProfScope ps_(PK_DZ, s);

@@ -7,7 +7,7 @@ namespace kd {
 
 struct DevStatus;
 
-enum EpiKind { EPI_FWD = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_ACC = 3, EPI_FWDZ = 4 };
+enum EpiKind { EPI_FWD = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_ACC = 3, EPI_FWDZ = 4, EPI_DZFWD = 5 };
 enum Order { ORDER_M_FAST = 0, ORDER_N_FAST = 1, ORDER_SPLIT = 2 };
 enum WaitSite { SITE_PROD = 1, SITE_MMA_FULL = 2, SITE_MMA_TEMPTY = 3, SITE_EPI = 4,
                 SITE_INJECT = 5, SITE_DRAIN = 6 };
@@ -17,6 +17,8 @@ struct GemmArgs {
   int kb_total;          // k-blocks of the whole reduction
   int order;             // Order
   int a_row0;            // y offset of A's TMA coordinates
+  int m_split;           // EPI_DZFWD: M tiles of the DZ part; tiles from m_split on are the FWD part
+  int a_row0_b;          // EPI_DZFWD: y offset of A for the FWD part's tiles
   int b_row0;            // y offset of B's TMA coordinates
   uint64_t timeout_ns;
   DevStatus* status;
@@ -31,9 +33,11 @@ struct EpiArgs {
   int out_row0;          // EPI_F32 / EPI_ACC / EPI_DZ: y offset of the output coordinates
   int split_rows;        // EPI_F32: y offset between the outputs of two K splits
   int first;             // EPI_ACC: store instead of add
-  // EPI_FWD / EPI_DZ
+  // EPI_FWD / EPI_DZ (EPI_DZFWD: grow0 / rows_valid for the DZ part, *_b for the FWD part)
   int K;                 // cached entries per token
   int grow0;             // global token index of chunk row 0
+  int grow0_b;           // EPI_DZFWD: global token index of the FWD part's chunk row 0
+  int rows_valid_b;      // EPI_DZFWD: valid rows of the FWD part's chunk
   int c_alloc;           // rows of the chunk scratch buffers
   const int* sid;        // [N][K] ids sorted ascending per row
   const float* sp;       // [N][K] teacher p in the same order

@@ -28,6 +28,10 @@
 //              in the tile, stored as bf16 through TMA (backward recompute).
 //   EPI_FWDZ : EPI_FWD, and z itself stored as fp32 through TMA (the
 //              logits kept for a backward pass without recompute).
+//   EPI_DZFWD: EPI_DZ on the M tiles below m_split (the recompute of one
+//              chunk) and EPI_FWD on the others (the forward of the next
+//              chunk): both multiply by all of W, which one launch then
+//              streams from memory once for the two.
 //   EPI_F32  : alpha * D stored as fp32 through TMA.
 //   EPI_ACC  : alpha * D added into an fp32 tensor by TMA reduce-add
 //              (plain store when `first`).
@@ -73,6 +77,8 @@ struct GemmCfg {
   static constexpr bool PACED = KIND == EPI_ACC || KIND == EPI_FWDZ;
   static constexpr int OUT_BOXES = BN / 32;   // fp32 32-column boxes per warp and tile
   static constexpr int EPI_BYTES = (KIND == EPI_FWD) ? 0 : 4 * 2 * EPI_STAGE_BYTES;
+  static constexpr bool HAS_FWD = KIND == EPI_FWD || KIND == EPI_FWDZ || KIND == EPI_DZFWD;
+  static constexpr bool HAS_DZ = KIND == EPI_DZ || KIND == EPI_DZFWD;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
@@ -234,6 +240,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int u = unit0; u < units; u += ustep) {
         const Unit t = unit_of(u, g);
         const int a_m0 = t.m * C::TILE_M + static_cast<int>(rank) * BM;
+        const int a_y0 = (C::KIND == EPI_DZFWD && t.m >= g.m_split) ? g.a_row0_b : g.a_row0;
         const int b_n0 = t.n * C::BN + static_cast<int>(rank) * (tile_cols(t.n) / C::NCTA);
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; kb += C::KSUB) {
@@ -250,10 +257,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int k0 = (kb + j) * BK;
             if constexpr (!C::CTA2) {
               if (!C::A_MN) {
-                tma_load_2d(a, &tmA, &full[stage], k0, g.a_row0 + a_m0);
+                tma_load_2d(a, &tmA, &full[stage], k0, a_y0 + a_m0);
               } else {
-                tma_load_2d(a, &tmA, &full[stage], a_m0, g.a_row0 + k0);
-                tma_load_2d(a + 8192, &tmA, &full[stage], a_m0 + 64, g.a_row0 + k0);
+                tma_load_2d(a, &tmA, &full[stage], a_m0, a_y0 + k0);
+                tma_load_2d(a + 8192, &tmA, &full[stage], a_m0 + 64, a_y0 + k0);
               }
               if (!C::B_MN) {
                 tma_load_2d(b, &tmB, &full[stage], k0, g.b_row0 + b_n0);
@@ -265,10 +272,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
               // both CTAs' bytes complete on the leader's full barrier
               if (!C::A_MN) {
-                tma_load_2d_pair(a, &tmA, fb, k0, g.a_row0 + a_m0);
+                tma_load_2d_pair(a, &tmA, fb, k0, a_y0 + a_m0);
               } else {
-                tma_load_2d_pair(a, &tmA, fb, a_m0, g.a_row0 + k0);
-                tma_load_2d_pair(a + 8192, &tmA, fb, a_m0 + 64, g.a_row0 + k0);
+                tma_load_2d_pair(a, &tmA, fb, a_m0, a_y0 + k0);
+                tma_load_2d_pair(a + 8192, &tmA, fb, a_m0 + 64, a_y0 + k0);
               }
               if (!C::B_MN) {
                 tma_load_2d_pair(b, &tmB, fb, k0, g.b_row0 + b_n0);
@@ -407,28 +414,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int acc = lt & 1;
       const uint32_t acc_par = (lt >> 1) & 1;
       const int slab0 = t.m * C::TILE_M + static_cast<int>(rank) * BM;   // first row of the slab
-      const int mrow = slab0 + row;                     // row within the launch's M range
-      const bool row_ok = mrow < e.rows_valid;
       const int box_row0 = slab0 + q * 32;              // first row of this warp's boxes
+      // EPI_DZFWD: which part this tile belongs to, and its rows within that
+      // part's chunk (the FWD part's tiles start at m_split)
+      const bool fwd_part = C::KIND == EPI_DZFWD ? t.m >= g.m_split : C::HAS_FWD;
+      const bool b_part = C::KIND == EPI_DZFWD && fwd_part;
+      const int mrow = b_part ? slab0 + row - g.m_split * C::TILE_M : slab0 + row;
+      const int grow0 = b_part ? e.grow0_b : e.grow0;
+      const bool row_ok = mrow < (b_part ? e.rows_valid_b : e.rows_valid);
 
       // per-row teacher lookups, issued before waiting on the accumulator
       int hit = 0, hit_end = 0, hit_col = 1 << 30;
       const int* ids = nullptr;
       float lse2 = 0.f;
       const int v0 = t.n * C::BN;
-      if constexpr (C::KIND == EPI_FWD || C::KIND == EPI_FWDZ || C::KIND == EPI_DZ) {
+      if constexpr (C::HAS_FWD || C::HAS_DZ) {
         if (row_ok) {
-          ids = e.sid + static_cast<long long>(e.grow0 + mrow) * e.K;
+          ids = e.sid + static_cast<long long>(grow0 + mrow) * e.K;
           hit = lower_bound_ids(ids, e.K, v0);
           hit_end = lower_bound_ids(ids, e.K, v0 + C::BN);
           if (hit < hit_end) hit_col = __ldg(ids + hit) - v0;
-          if constexpr (C::KIND == EPI_DZ) lse2 = __ldg(e.lse2 + mrow);
+          if (C::HAS_DZ && !fwd_part) lse2 = __ldg(e.lse2 + mrow);
         }
       }
-      // EPI_DZ: a masked token's dZ row is zero
+      // DZ: a masked token's dZ row is zero
       bool row_live = row_ok;
-      if constexpr (C::KIND == EPI_DZ) {
-        if (row_ok && e.mask && __ldg(e.mask + e.grow0 + mrow) == 0) {
+      if constexpr (C::HAS_DZ) {
+        if (!fwd_part && row_ok && e.mask && __ldg(e.mask + grow0 + mrow) == 0) {
           row_live = false;
           hit_col = 1 << 30;
         }
@@ -441,101 +453,103 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       const uint32_t tb = tmem_base + lane_off + acc * C::BN;
 
-      if constexpr (C::KIND == EPI_FWD || C::KIND == EPI_FWDZ) {
-        float m_run = -INFINITY, s_run = 0.f;
+      if constexpr (C::HAS_FWD || C::HAS_DZ) {
+        if (C::HAS_FWD && fwd_part) {
+          float m_run = -INFINITY, s_run = 0.f;
 #pragma unroll 1
-        for (int b = 0; b < C::BN / 32; ++b) {
-          uint32_t r[32];
-          tmem_ld32(tb + b * 32, r);
-          tmem_ld_wait();
-          reg_fence(r);
-          const int c0 = b * 32;
-          // gather z at the cached ids that fall in these 32 columns
-          while (hit_col < c0 + 32) {
-            const float z = select32(r, hit_col - c0);
-            e.zg[static_cast<long long>(mrow) * e.K + hit] = z;
-            if (e.dbg_found) {
-              const long long gr = static_cast<long long>(e.grow0 + mrow) * e.K;
-              e.dbg_found[gr + __ldg(e.perm + gr + hit)] = v0 + hit_col;
-            }
-            ++hit;
-            hit_col = (hit < hit_end) ? __ldg(ids + hit) - v0 : (1 << 30);
-          }
-          const int nvalid = e.cols_valid - (v0 + c0);   // warp-uniform
-          if (nvalid <= 0) continue;
-          if constexpr (C::KIND == EPI_FWDZ) {
-            if (box_row0 < e.c_alloc) {                  // warp-uniform: inside the z tensor
-              pace(b);
-              const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
-              if (lane == 0) bulk_wait_read<1>();
-              __syncwarp();
-              stage_row_128B(box, lane, r);
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, box_row0);
-                bulk_commit();
+          for (int b = 0; b < C::BN / 32; ++b) {
+            uint32_t r[32];
+            tmem_ld32(tb + b * 32, r);
+            tmem_ld_wait();
+            reg_fence(r);
+            const int c0 = b * 32;
+            // gather z at the cached ids that fall in these 32 columns
+            while (hit_col < c0 + 32) {
+              const float z = select32(r, hit_col - c0);
+              e.zg[static_cast<long long>(mrow) * e.K + hit] = z;
+              if (e.dbg_found) {
+                const long long gr = static_cast<long long>(grow0 + mrow) * e.K;
+                e.dbg_found[gr + __ldg(e.perm + gr + hit)] = v0 + hit_col;
               }
-              ++sub_ctr;
+              ++hit;
+              hit_col = (hit < hit_end) ? __ldg(ids + hit) - v0 : (1 << 30);
             }
+            const int nvalid = e.cols_valid - (v0 + c0);   // warp-uniform
+            if (nvalid <= 0) continue;
+            if constexpr (C::KIND == EPI_FWDZ) {
+              if (box_row0 < e.c_alloc) {                  // warp-uniform: inside the z tensor
+                pace(b);
+                const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                stage_row_128B(box, lane, r);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, box_row0);
+                  bulk_commit();
+                }
+                ++sub_ctr;
+              }
+            }
+            float bm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nvalid) bm = fmaxf(bm, __uint_as_float(r[j]));
+            const float m_new = fmaxf(m_run, bm * e.scale2);
+            float s = s_run * ex2_approx(m_run - m_new);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nvalid) s += ex2_approx(fmaf(__uint_as_float(r[j]), e.scale2, -m_new));
+            s_run = s;
+            m_run = m_new;
           }
-          float bm = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nvalid) bm = fmaxf(bm, __uint_as_float(r[j]));
-          const float m_new = fmaxf(m_run, bm * e.scale2);
-          float s = s_run * ex2_approx(m_run - m_new);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nvalid) s += ex2_approx(fmaf(__uint_as_float(r[j]), e.scale2, -m_new));
-          s_run = s;
-          m_run = m_new;
-        }
-        release_acc(acc);
-        if (row_ok) e.part[static_cast<long long>(t.n) * e.c_alloc + mrow] = make_float2(m_run, s_run);
-      } else if constexpr (C::KIND == EPI_DZ) {
-        const bool box_ok = box_row0 < e.c_alloc;       // warp-uniform: inside the dZ tensor
+          release_acc(acc);
+          if (row_ok) e.part[static_cast<long long>(t.n) * e.c_alloc + mrow] = make_float2(m_run, s_run);
+        } else if constexpr (C::HAS_DZ) {
+          const bool box_ok = box_row0 < e.c_alloc;       // warp-uniform: inside the dZ tensor
 #pragma unroll 1
-        for (int sb = 0; sb < C::BN / 64; ++sb) {
-          const int c0 = sb * 64;
-          if (v0 + c0 >= e.cols_valid) break;            // warp-uniform
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tb + c0, r0);
-          tmem_ld32(tb + c0 + 32, r1);
-          tmem_ld_wait();
-          reg_fence(r0);
-          reg_fence(r1);
-          if (!box_ok) continue;
-          float gv[64];
+          for (int sb = 0; sb < C::BN / 64; ++sb) {
+            const int c0 = sb * 64;
+            if (v0 + c0 >= e.cols_valid) break;            // warp-uniform
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tb + c0, r0);
+            tmem_ld32(tb + c0 + 32, r1);
+            tmem_ld_wait();
+            reg_fence(r0);
+            reg_fence(r1);
+            if (!box_ok) continue;
+            float gv[64];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            gv[j] = row_live ? ex2_approx(fmaf(__uint_as_float(r0[j]), e.scale2, -lse2)) : 0.f;
-            gv[32 + j] = row_live ? ex2_approx(fmaf(__uint_as_float(r1[j]), e.scale2, -lse2)) : 0.f;
-          }
-          while (hit_col < c0 + 64) {
-            const float p = __ldg(e.sp + static_cast<long long>(e.grow0 + mrow) * e.K + hit);
-            const int jj = hit_col - c0;
+            for (int j = 0; j < 32; ++j) {
+              gv[j] = row_live ? ex2_approx(fmaf(__uint_as_float(r0[j]), e.scale2, -lse2)) : 0.f;
+              gv[32 + j] = row_live ? ex2_approx(fmaf(__uint_as_float(r1[j]), e.scale2, -lse2)) : 0.f;
+            }
+            while (hit_col < c0 + 64) {
+              const float p = __ldg(e.sp + static_cast<long long>(grow0 + mrow) * e.K + hit);
+              const int jj = hit_col - c0;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) gv[j] -= (j == jj) ? p : 0.f;
-            ++hit;
-            hit_col = (hit < hit_end) ? __ldg(ids + hit) - v0 : (1 << 30);
-          }
-          uint32_t pk[32];
+              for (int j = 0; j < 64; ++j) gv[j] -= (j == jj) ? p : 0.f;
+              ++hit;
+              hit_col = (hit < hit_end) ? __ldg(ids + hit) - v0 : (1 << 30);
+            }
+            uint32_t pk[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(gv[2 * j], gv[2 * j + 1]);
-          const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-          stage_row_128B(box, lane, pk);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, e.out_row0 + box_row0);
-            bulk_commit();
+            for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(gv[2 * j], gv[2 * j + 1]);
+            const uint32_t box = stage_base + (sub_ctr & 1u) * EPI_STAGE_BYTES;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            stage_row_128B(box, lane, pk);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, sEpi + (box - smem_u32(sEpi)), v0 + c0, e.out_row0 + box_row0);
+              bulk_commit();
+            }
+            ++sub_ctr;
           }
-          ++sub_ctr;
+          release_acc(acc);
         }
-        release_acc(acc);
       } else {
         // EPI_F32 / EPI_ACC: alpha * D -> fp32, 32-column boxes
         const bool box_ok = box_row0 < e.rows_valid;    // warp-uniform

@@ -31,6 +31,7 @@ enum GemmVariant {
   GV_TEST_MM2 = 15,
   GV_FWDZ = 16,        // K1 that also stores the chunk's fp32 logits
   GV_TEST_KK2S = 17,   // pair, K-major operands, two k-blocks per ring stage
+  GV_DZFWD = 18,       // K3 of chunk j and K1 of chunk j+1 in one launch (W streamed once)
 };
 
 // Tile width of the N dimension of each variant.

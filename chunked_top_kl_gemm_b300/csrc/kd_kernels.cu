@@ -40,6 +40,8 @@ namespace kd {
 // The gradient GEMMs wait on DRAM-fed operands and keep finer stages.
 using CfgFwd = GemmCfg<256, false, false, 3, EPI_FWD, true, 2>;
 using CfgDz = GemmCfg<256, false, false, 3, EPI_DZ, true, 2>;
+// the recompute of one chunk and the forward of the next in one launch
+using CfgDzFwd = GemmCfg<256, false, false, 3, EPI_DZFWD, true, 2>;
 using CfgGradH = GemmCfg<256, true, false, 6, EPI_F32, true>;   // grad_hidden^T = W^T dZ^T
 using CfgGradW = GemmCfg<256, true, false, 6, EPI_ACC, true>;   // grad_W = dZ^T h_c
 // forward that also keeps the chunk's fp32 logits (backward without recompute)
@@ -150,7 +152,8 @@ static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const 
   X(GV_TEST_MM, CfgTestMM) X(GV_TEST_KK192, CfgTestKK192) X(GV_TEST_KM256, CfgTestKM256) \
   X(GV_TEST_MK256, CfgTestMK256) X(GV_TEST_MM256, CfgTestMM256)                         \
   X(GV_TEST_KK2, CfgTestKK2) X(GV_TEST_KM2, CfgTestKM2) X(GV_TEST_MK2, CfgTestMK2)       \
-  X(GV_TEST_MM2, CfgTestMM2) X(GV_FWDZ, CfgFwdZ) X(GV_TEST_KK2S, CfgTestKK2S)
+  X(GV_TEST_MM2, CfgTestMM2) X(GV_FWDZ, CfgFwdZ) X(GV_TEST_KK2S, CfgTestKK2S)              \
+  X(GV_DZFWD, CfgDzFwd)
 
 int gemm_bn(int variant) {
 #define X(V, C) case V: return C::BN;
