@@ -101,7 +101,7 @@ def _block(rng_):
     return r0, out["lse"], out["loss_rows"], out["grad_W_rows"]
 
 
-# ------------------------------------------------------------------ driver
+# ------------------------------------------------------------------ per workload
 def make(name: str, workers: int, block: int, tmp_root: str) -> None:
     import oracle
     import workloads

@@ -193,22 +193,36 @@ def make_inputs_host(cfg: Config, seed: int = 0,
     rng = np.random.Generator(np.random.PCG64(seed))
     # normal draws in float64 (numpy's fast path), rounded to fp32, in row
     # blocks to bound the temporaries; consecutive blocks continue the stream
-    hidden = np.empty((N, H), dtype=np.float32)
+    # (block buffers reused across blocks: the same draws and operations as
+    # whole-array temporaries, without fresh allocations; each block is
+    # rounded fp32 -> bf16 into the output)
+    B = min(_HOST_BLOCK, max(N, V))
+    buf = np.empty((B, H))
+    tmp = np.empty_like(buf)
+    b32 = np.empty((B, H), dtype=np.float32)
+    hidden_t = torch.empty((N, H), dtype=torch.bfloat16)
     for r0 in range(0, N, _HOST_BLOCK):
-        blk = rng.standard_normal((min(N, r0 + _HOST_BLOCK) - r0, H))
+        rows = min(N, r0 + _HOST_BLOCK) - r0
+        blk, h32 = buf[:rows], b32[:rows]
+        rng.standard_normal(out=blk)
+        h32[...] = blk                                    # rounded to fp32
         if cfg.hidden_rms_norm:
             # each row divided by its RMS (computed from the fp32 values)
-            blk = blk.astype(np.float32).astype(np.float64)
-            blk = blk / np.sqrt((blk * blk).sum(axis=1, keepdims=True) / H)
-        hidden[r0:r0 + blk.shape[0]] = blk
-    hidden_t = torch.from_numpy(hidden).to(torch.bfloat16)
-    del hidden
-    W = np.empty((V, H), dtype=np.float32)
+            blk[...] = h32
+            np.multiply(blk, blk, out=tmp[:rows])
+            rms = np.sqrt(tmp[:rows].sum(axis=1, keepdims=True) / H)
+            np.divide(blk, rms, out=tmp[:rows])
+            h32[...] = tmp[:rows]
+        hidden_t[r0:r0 + rows] = torch.from_numpy(h32).to(torch.bfloat16)
+    W_t = torch.empty((V, H), dtype=torch.bfloat16)
     for r0 in range(0, V, _HOST_BLOCK):
-        blk = rng.standard_normal((min(V, r0 + _HOST_BLOCK) - r0, H)).astype(np.float32)
-        W[r0:r0 + blk.shape[0]] = blk * np.float32(cfg.w_std)
-    W_t = torch.from_numpy(W).to(torch.bfloat16)
-    del W
+        rows = min(V, r0 + _HOST_BLOCK) - r0
+        w32 = b32[:rows]
+        rng.standard_normal(out=buf[:rows])
+        w32[...] = buf[:rows]                             # rounded to fp32
+        np.multiply(w32, np.float32(cfg.w_std), out=w32)
+        W_t[r0:r0 + rows] = torch.from_numpy(w32).to(torch.bfloat16)
+    del buf, tmp, b32
     idx = _distinct_ids_host(rng, N, K, V)
     if cfg.teacher == "exp_gaps":
         gaps = rng.exponential(scale=cfg.gap_scale, size=(N, K - 1))
@@ -262,7 +276,7 @@ def input_digest(inp: dict) -> str:
         if t.dtype == torch.bfloat16:
             t = t.view(torch.int16)
         h.update(key.encode())
-        h.update(t.numpy().tobytes())
+        h.update(t.numpy())            # the array's bytes, without a copy
     return h.hexdigest()
 
 
