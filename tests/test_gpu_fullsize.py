@@ -188,3 +188,33 @@ def test_full_vocab_head_single_chunk():
     err = rel_l2(got["grad_W"][vrows], want["grad_W"][vrows])
     assert err <= GRAD_REL_L2, err
     assert rel_l2(got["grad_W"], want["grad_W"]) <= GRAD_REL_L2
+
+
+@pytest.mark.parametrize("flag", ["min_scratch", "store_logits"])
+def test_gptoss32k_other_plans_against_oracle(flag):
+    """gptoss32k with grad_W per chunk (KD_FLAG_MIN_SCRATCH) and with the
+    stored-logits backward: the same stored oracle values hold for every
+    plan (loss, every token's KL term, the grad_W rows)."""
+    ensure_lib()
+    cfg = workloads.CONFIGS["gptoss32k"]
+    fx = load_fixture("gptoss32k")
+    inp_cpu = workloads.make_inputs_host(cfg, seed=int(fx["seed"]))
+    assert workloads.input_digest(inp_cpu) == str(fx["digest"])
+    inp = to_device(inp_cpu)
+    flags = {"min_scratch": kd.KD_FLAG_MIN_SCRATCH, "store_logits": kd.KD_FLAG_STORE_LOGITS}[flag]
+    N, H, V, K = cfg.N, cfg.H, cfg.V, cfg.K
+    gh = torch.empty((N, H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, cfg.chunk, flags),
+                     dtype=torch.uint8, device="cuda")
+    loss = kd.kd_topk_kl_fwd_bwd_flags(inp["hidden"], inp["W"], inp["topk_idx"],
+                                       inp["topk_logit"], None, cfg.T, cfg.chunk, flags, gh, gW,
+                                       ws)
+    torch.cuda.synchronize()
+    del ws
+    want_loss = float(fx["loss"])
+    assert abs(loss - want_loss) <= LOSS_RTOL * abs(want_loss), (loss, want_loss)
+    vrows = torch.from_numpy(fx["vrows"]).to(gW.device)
+    err = rel_l2(gW[vrows].cpu().numpy(), fx["grad_W_rows"].astype(np.float64))
+    assert err <= GRAD_REL_L2, err
+    assert torch.isfinite(gh).all()
