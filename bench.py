@@ -405,9 +405,12 @@ def run_gpu(args):
     tflops = flops_step * args.steps / t_max / 1e12
 
     # end to end: every step's inputs are copied from pinned host memory and
-    # its loss is read back, as a training loop feeding the loss would do it:
-    # the next step's inputs are copied on a second stream into a second set
-    # of device buffers while the current step computes
+    # its loss (and status word) is read back into pinned host memory, as a
+    # training loop feeding the loss would do it, through the library's
+    # asynchronous entry point (no host synchronisation per step).  The next
+    # step's inputs are copied on a second stream into a second set of
+    # device buffers while the current step computes; a buffer set is
+    # refilled only after the step that read it has passed on the GPU.
     h_host = h.cpu().pin_memory()
     idx_host = idx.cpu().pin_memory()
     lg_host = lg.cpu().pin_memory()
@@ -415,27 +418,35 @@ def run_gpu(args):
     bufs = [(h, idx, lg), (torch.empty_like(h), torch.empty_like(idx), torch.empty_like(lg))]
     copy_stream = torch.cuda.Stream(dev)
     ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    loss_dev = torch.zeros(1, dtype=torch.float32, device=dev)
+    status_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_read = max(args.steps, 2)
+    loss_host = torch.zeros(n_read, dtype=torch.float32).pin_memory()
+    status_host = torch.zeros(n_read, dtype=torch.int32).pin_memory()
 
-    def copy_in(slot):
+    def copy_in(slot, first):
         with torch.cuda.stream(copy_stream):
+            if not first:
+                copy_stream.wait_event(done[slot])     # the step that read this set passed
             for dst, src in zip(bufs[slot], (h_host, idx_host, lg_host)):
                 dst.copy_(src, non_blocking=True)
             ready[slot].record(copy_stream)
 
     def e2e_steps(n):
-        copy_in(0)
+        copy_in(0, True)
         for i in range(n):
             slot = i % 2
             stream.wait_event(ready[slot])
             if i + 1 < n:
-                copy_in(1 - slot)   # the other buffers are free: their step has returned
+                copy_in(1 - slot, i == 0)
             hb, ib, lb = bufs[slot]
-            if flags:
-                kd.kd_topk_kl_fwd_bwd_flags(hb, W, ib, lb, None, T, chunk, flags, gh, gW, ws,
-                                            stream=stream)
-            else:
-                # synchronises the stream and returns the loss to the host
-                kd.kd_topk_kl_fwd_bwd_ex(hb, W, ib, lb, T, chunk, gh, gW, ws, stream=stream)
+            kd.kd_topk_kl_fwd_bwd_async(hb, W, ib, lb, None, T, chunk, flags, loss_dev,
+                                        status_dev, gh, gW, ws, stream=stream)
+            done[slot].record(stream)
+            with torch.cuda.stream(stream):
+                loss_host[i].copy_(loss_dev[0], non_blocking=True)
+                status_host[i].copy_(status_dev[0], non_blocking=True)
 
     e2e_steps(2)
     dist_barrier(dev)
@@ -445,6 +456,10 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     t_e2e = dist_max(time.perf_counter() - w0, dev)
     dist_barrier(dev)
+    if int(status_host[:args.steps].abs().sum()) != 0:
+        raise RuntimeError(f"end-to-end steps reported device status {status_host.tolist()}")
+    if not bool(torch.isfinite(loss_host[:args.steps]).all()):
+        raise RuntimeError("end-to-end steps returned a non-finite loss")
 
     if rank != 0:
         if world > 1:
@@ -505,7 +520,8 @@ def run_gpu(args):
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clk,
         "e2e": {"value": throughput(N, args.steps, world, t_e2e), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8,
+                "api": "kd_topk_kl_fwd_bwd_async, loss and status read back every step"},
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
