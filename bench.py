@@ -515,6 +515,13 @@ def run_gpu(args):
                                "event profiler on (not the headline loop)"},
         "kernels": {k: {"ms_per_step": v[0] / prof_steps, "launches_per_step": v[1] / prof_steps}
                     for k, v in prof.items() if v[1] > 0},
+        # every GEMM kind against the same sustained peak (its share of the
+        # 8NHV flops over its event time)
+        "gemm_rooflines": {k: {"tflops": gemm_flops_per_step(k, N, H, V, chunk, args.store_logits)
+                                         / (v[0] / prof_steps / 1e3) / 1e12,
+                               "frac": gemm_flops_per_step(k, N, H, V, chunk, args.store_logits)
+                                       / (v[0] / prof_steps / 1e3) / 1e12 / peak_sust}
+                           for k, v in gemm.items()},
         "profile_pass": {"steps": prof_steps, "ms_per_step": t_prof / prof_steps * 1e3,
                          "clocks": pclk},
         "gpu_launches": int(round(launches_per_step * args.steps)),
