@@ -6,7 +6,7 @@ training step can keep the host out of the loop or be captured in a CUDA
 graph.  Checked here:
 
 * it gives bit for bit the blocking call's loss and gradients (plain,
-  masked, accumulating, stored logits);
+  masked, accumulating, stored logits, per-chunk grad_W, masked per-chunk);
 * a captured graph replayed on new inputs written into the same buffers
   matches a blocking call on those inputs, and the float64 oracle;
 * an accumulating masked graph replayed twice adds two steps' gradients;
@@ -61,14 +61,17 @@ def _mask(N, frac, seed):
     return m.cuda()
 
 
-@pytest.mark.parametrize("mode", ["plain", "masked", "accumulate", "store_logits"])
+@pytest.mark.parametrize("mode", ["plain", "masked", "accumulate", "store_logits", "min_scratch",
+                                  "masked_min_scratch"])
 @pytest.mark.parametrize("cfg", [MID, RAGGED], ids=["mid", "ragged"])
 def test_async_equals_blocking_bitwise(cfg, mode):
     ensure_lib()
     inp = to_device(workloads.make_inputs(cfg, seed=31))
-    mask = _mask(cfg.N, 0.6, seed=5) if mode == "masked" else None
+    mask = _mask(cfg.N, 0.6, seed=5) if mode.startswith("masked") else None
     flags = {"accumulate": kd.KD_FLAG_ACCUMULATE,
-             "store_logits": kd.KD_FLAG_STORE_LOGITS}.get(mode, 0)
+             "store_logits": kd.KD_FLAG_STORE_LOGITS,
+             "min_scratch": kd.KD_FLAG_MIN_SCRATCH,
+             "masked_min_scratch": kd.KD_FLAG_MIN_SCRATCH}.get(mode, 0)
     a, b = _bufs(cfg, flags), _bufs(cfg, flags)
     if mode == "accumulate":
         g = torch.Generator(device="cuda").manual_seed(2)
