@@ -36,11 +36,11 @@ constexpr unsigned kAllFlags = KD_FLAG_ACCUMULATE | KD_FLAG_STORE_LOGITS | KD_FL
 // bracketed by two CUDA events on the launch stream; after the call's final
 // synchronisation the elapsed times are added to per-kind totals.
 enum ProfKind { PK_PREP = 0, PK_FWD, PK_LSE, PK_DZ, PK_GRAD_H, PK_SPLIT_RED, PK_GRAD_W,
-                PK_FINAL, PK_TRANSPOSE, PK_MASK, PK_DZ_EW, PK_CACHE_GEMM, PK_CACHE_SELECT,
+                PK_FINAL, PK_MASK, PK_DZ_EW, PK_CACHE_GEMM, PK_CACHE_SELECT,
                 PK_DZ_FWD, PK_COUNT };
 const char* const kProfNames[PK_COUNT] = {"prep_topk", "gemm_fwd_lse_gather", "lse_loss_fold",
                                           "gemm_bwd_dz", "gemm_grad_hidden", "split_reduce",
-                                          "gemm_grad_W", "loss_final", "transpose_chunk",
+                                          "gemm_grad_W", "loss_final",
                                           "mask_count", "dz_from_logits", "cache_gemm_logits",
                                           "cache_topk_select", "gemm_dz_and_next_fwd"};
 
@@ -162,7 +162,7 @@ struct Plan {
   int sms;
   bool store_z;   // keep each chunk's fp32 logits instead of recomputing them
   size_t off_status, off_sid, off_sp, off_perm, off_ent, off_psum, off_loss_rows, off_lse2,
-      off_zg, off_part, off_dz, off_k4, off_hT, off_z, total;
+      off_zg, off_part, off_dz, off_k4, off_z, total;
 };
 
 bool sizes_ok(long long N, int H, int V, int K, int chunk) {
@@ -226,7 +226,6 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_
   p.off_part = take(sizeof(float2) * p.vt * c);
   p.off_dz = take(2ull * p.gg * c * V);
   p.off_k4 = take(4ull * p.splits * p.hp * c);
-  p.off_hT = take(2ull * H * p.gg * c);
   p.off_z = store_z ? take(4ull * c * V) : 0;
   p.total = o;
   return p;
@@ -315,7 +314,6 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   float2* part = reinterpret_cast<float2*>(base + p.off_part);
   void* dz = base + p.off_dz;
   float* k4 = reinterpret_cast<float*>(base + p.off_k4);
-  void* hT = base + p.off_hT;
   float* zbuf = store_z ? reinterpret_cast<float*>(base + p.off_z) : nullptr;
 
   const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
@@ -327,7 +325,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   // TMA descriptors
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  CUtensorMap tm_hid_k, tm_w_k, tm_dz_st, tm_dz_k256, tm_w_mn, tm_k4_st, tm_dz_mn, tm_ht_k, tm_gw;
+  CUtensorMap tm_hid_k, tm_w_k, tm_dz_st, tm_dz_k256, tm_w_mn, tm_k4_st, tm_dz_mn, tm_hid_mn, tm_gw;
   bool ok = true;
   ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
   ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, b_box_rows(kd::GV_FWD));
@@ -337,7 +335,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   ok &= make_map(&tm_w_mn, BF16, 2, W, H, V, 64, 64);
   ok &= make_map(&tm_k4_st, F32, 4, k4, p.chunk, static_cast<uint64_t>(p.splits) * p.hp, 32, 32);
   ok &= make_map(&tm_dz_mn, BF16, 2, dz, V, dz_rows, 64, 64);
-  ok &= make_map(&tm_ht_k, BF16, 2, hT, dz_rows, H, 64, b_box_rows(kd::GV_GRAD_W));
+  ok &= make_map(&tm_hid_mn, BF16, 2, hidden, H, N, 64, 64);       // MN-major B of grad_W
   ok &= make_map(&tm_gw, F32, 4, gW, H, V, 32, 32);
   CUtensorMap tm_z_st;
   if (store_z) ok &= make_map(&tm_z_st, F32, 4, zbuf, V, p.chunk, 32, 32);
@@ -366,7 +364,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
     const int row0 = j * p.chunk;
     const int cj = static_cast<int>(std::min<long long>(p.chunk, N - row0));
     const int mt = static_cast<int>(cdiv(cj, kd::gemm_tile_m(kd::GV_FWD)));
-    // this chunk's dZ rows and h_c^T columns: slot `slot` of its grad_W group
+    // this chunk's dZ rows: slot `slot` of its grad_W group
     const int slot = j % p.gg;
     const int slot_row0 = slot * p.chunk;
     uint8_t* dz_slot = static_cast<uint8_t*>(dz) + 2ull * slot_row0 * V;
@@ -444,25 +442,22 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
                                     static_cast<long long>(p.hp) * p.chunk, p.chunk, cj, H, alpha, alpha_dev, accumulate,
                                     gh + static_cast<long long>(row0) * H, s)); }
 
-    // h_c^T (B operand of grad_W, K-major) into the slot's columns
-    { ProfScope ps_(PK_TRANSPOSE, s); KD_CUDA(kd::launch_transpose_chunk(
-          static_cast<const uint8_t*>(hidden) + 2ull * row0 * H, cj, p.chunk, H,
-          static_cast<uint8_t*>(hT) + 2ull * slot_row0, static_cast<int>(dz_rows), s)); }
-
-    // grad_W += dZ_g^T h_g over the group's rows, once its last chunk is in
+    // grad_W += dZ_g^T h_g over the group's rows, once its last chunk is in.
+    // B is the group's hidden rows read MN-major; k-blocks past the group's
+    // rows meet zero dZ rows, or hidden rows past N (zero-filled)
     if (slot + 1 < p.gg && j + 1 < p.n_chunks) continue;
     const int grp_rows = slot_row0 + cj;   // only the call's last chunk is partial
     kd::GemmArgs g3{};
     g3.m_tiles = static_cast<int>(cdiv(V, kd::gemm_tile_m(kd::GV_GRAD_W))); g3.n_tiles = p.ht;
     g3.splits = 1;
     g3.kb_total = static_cast<int>(cdiv(grp_rows, 64));
-    g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = 0;
+    g3.order = kd::ORDER_N_FAST; g3.a_row0 = 0; g3.b_row0 = row0 - slot_row0;
     g3.timeout_ns = timeout; g3.status = dst; g3.inject_timeout = (j == p.gg - 1 && inject == 4);
     kd::EpiArgs e3{};
     e3.rows_valid = V; e3.cols_valid = H; e3.alpha = alpha; e3.out_row0 = 0;
     e3.alpha_dev = alpha_dev;
     e3.first = (j - slot == 0) && !accumulate;
-    { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_ht_k, tm_gw, g3, e3, s)); }
+    { ProfScope ps_(PK_GRAD_W, s); KD_CUDA(kd::launch_gemm(kd::GV_GRAD_W, tm_dz_mn, tm_hid_mn, tm_gw, g3, e3, s)); }
   }
   kd::FinalOut fo{};
   if (async) fo = kd::FinalOut{loss_dev, status_dev, mask ? 1 : 0, KD_ERR_TIMEOUT, KD_ERR_INDEX};

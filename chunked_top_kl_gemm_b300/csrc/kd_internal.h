@@ -16,7 +16,7 @@ enum GemmVariant {
   GV_FWD = 0,       // K1: hidden_c * W^T, forward epilogue (lse partials + gather)
   GV_DZ = 1,        // K3: hidden_c * W^T recomputed, dZ epilogue (bf16 store)
   GV_GRAD_H = 2,    // K4: (dZ W)^T = W^T dZ^T (A MN-major), fp32 split-K partials
-  GV_GRAD_W = 3,    // K5: dZ^T * hidden_c (A MN-major, B = h_c^T K-major), fp32 reduce-add
+  GV_GRAD_W = 3,    // K5: dZ^T * hidden (A and B MN-major), fp32 reduce-add
   GV_TEST_KK = 4,   // test GEMMs: fp32 store, all four major combinations
   GV_TEST_KM = 5,
   GV_TEST_MK = 6,
@@ -83,9 +83,6 @@ cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_
 cudaError_t launch_mask_count(const uint8_t* mask, long long N, float T, DevStatus* st,
                               cudaStream_t s);
 
-// hT[h * ld + r] = hid[r][h] for the chunk's rows (zeros up to c_alloc)
-cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
-                                   int ld, cudaStream_t s);
 
 // Device-side results of an asynchronous call (loss == nullptr: none).
 struct FinalOut {

@@ -21,8 +21,8 @@
 //   GEMM GRAD_H   split-K  (G W)^T = W^T G^T -> fp32 partials [split][H][c];
 //                 split_reduce_t sums them, transposes and scales by 1/(T N)
 //                 into grad_hidden
-//   transpose     h_c^T (bf16) for the next GEMM's K-major operand
-//   GEMM GRAD_W   G^T h_c scaled by 1/(T N), TMA reduce-added into grad_W
+//   GEMM GRAD_W   G^T h scaled by 1/(T N) over a pair of chunks' rows (h read
+//                 MN-major), TMA reduce-added into grad_W
 //   loss_final    ordered sum of the per-token terms
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -43,7 +43,7 @@ using CfgDz = GemmCfg<256, false, false, 3, EPI_DZ, true, 2>;
 // the recompute of one chunk and the forward of the next in one launch
 using CfgDzFwd = GemmCfg<256, false, false, 3, EPI_DZFWD, true, 2>;
 using CfgGradH = GemmCfg<256, true, false, 6, EPI_F32, true>;   // grad_hidden^T = W^T dZ^T
-using CfgGradW = GemmCfg<256, true, false, 6, EPI_ACC, true>;   // grad_W = dZ^T h_c
+using CfgGradW = GemmCfg<256, true, true, 6, EPI_ACC, true>;    // grad_W = dZ^T h_c (h_c MN-major)
 // forward that also keeps the chunk's fp32 logits (backward without recompute)
 using CfgFwdZ = GemmCfg<256, false, false, 3, EPI_FWDZ, true, 2>;
 // single-CTA forms (128 x BN tiles), kept for the GEMM-core tests
@@ -459,52 +459,6 @@ cudaError_t launch_split_reduce_t(const float* part, int splits, long long split
   dim3 grid((rows_valid + SR_R - 1) / SR_R, (H + SR_H - 1) / SR_H);
   kd_split_reduce_t<<<grid, 256, 0, s>>>(part, splits, split_stride, c_alloc, rows_valid, H,
                                          alpha, alpha_dev, accumulate, out);
-  return cudaGetLastError();
-}
-
-// ------------------------------------------------------------------ chunk transpose
-// hT[h * ld + r] = hidden[r][h] for r < rows_valid, 0 for rows_valid <= r <
-// c_alloc (bf16; 64 x 64 tiles through shared memory, two elements per
-// access).  ld >= c_alloc is the row length of the whole h^T buffer, which
-// holds the columns of several chunks.
-__global__ void __launch_bounds__(256) kd_transpose_chunk(const __nv_bfloat16* __restrict__ hid,
-                                                          int rows_valid, int c_alloc, int H,
-                                                          int ld,
-                                                          __nv_bfloat16* __restrict__ hT) {
-  __shared__ __nv_bfloat16 tile[64][64 + 2];
-  const int r0 = blockIdx.x * 64, h0 = blockIdx.y * 64;
-  const int t = threadIdx.x;
-  const int h2 = (t & 31) * 2;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = (t >> 5) + 8 * i;
-    const int r = r0 + rr, h = h0 + h2;          // H is a multiple of 8: h, h+1 both valid
-    __nv_bfloat162 v = __floats2bfloat162_rn(0.f, 0.f);
-    if (r < rows_valid && h < H)
-      v = *reinterpret_cast<const __nv_bfloat162*>(hid + static_cast<long long>(r) * H + h);
-    tile[rr][h2] = v.x;
-    tile[rr][h2 + 1] = v.y;
-  }
-  __syncthreads();
-  const int r2 = (t & 31) * 2;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int hh = (t >> 5) + 8 * i;
-    const int h = h0 + hh, r = r0 + r2;          // c_alloc is a multiple of 128
-    if (h < H && r < c_alloc) {
-      __nv_bfloat162 v;
-      v.x = tile[r2][hh];
-      v.y = tile[r2 + 1][hh];
-      *reinterpret_cast<__nv_bfloat162*>(hT + static_cast<long long>(h) * ld + r) = v;
-    }
-  }
-}
-
-cudaError_t launch_transpose_chunk(const void* hid, int rows_valid, int c_alloc, int H, void* hT,
-                                   int ld, cudaStream_t s) {
-  dim3 grid((c_alloc + 63) / 64, (H + 63) / 64);
-  kd_transpose_chunk<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hid), rows_valid,
-                                          c_alloc, H, ld, static_cast<__nv_bfloat16*>(hT));
   return cudaGetLastError();
 }
 
