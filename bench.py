@@ -550,6 +550,69 @@ SWEEP_POINTS = (
 )
 
 
+def _sweep_point(kd, cfg, chunk, flags, dev, peaks):
+    """Peak memory and power-capped throughput of one call plan on one
+    workload: the inputs drawn on the device, one cold call for the peak,
+    then enough timed steps for about 1.5 s of clock samples.  Returns the
+    JSON fields, or a `skipped` reason when the plan's buffers would not fit
+    in 85 % of the device memory that is free."""
+    import torch
+
+    import workloads
+
+    N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    ws_bytes = kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, flags)
+    need = ws_bytes + sum(workloads.bytes_of_inputs(cfg).values()) + 4 * (N * H + V * H)
+    free, _ = torch.cuda.mem_get_info(dev)
+    if need > 0.85 * free:
+        return {"skipped": f"needs {need / 2**30:.1f} GiB, {free / 2**30:.1f} GiB free",
+                "needs_gib": need / 2**30}
+    mem0 = torch.cuda.memory_allocated(dev)
+    inp = workloads.make_inputs(cfg, seed=0, device=dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)     # not the input draw's temporaries
+    gh = torch.empty((N, H), dtype=torch.float32, device=dev)
+    gW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    h_, W_, i_, l_ = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
+
+    def call():
+        return kd.kd_topk_kl_fwd_bwd_flags(h_, W_, i_, l_, None, T, chunk, flags, gh, gW, ws)
+    loss = call()
+    torch.cuda.synchronize(dev)
+    peak = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
+    # time one more warm call, then enough steps for ~1.5 s of samples
+    w0 = time.perf_counter()
+    call()
+    steps = max(3, min(200, int(1.5 / max(time.perf_counter() - w0, 1e-4)) + 1))
+    clocks = ClockSampler(_gpu_id(0))
+    clocks.start()
+    time.sleep(0.2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        loss = call()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    flops = cfg.flops * (0.75 if flags & kd.KD_FLAG_STORE_LOGITS else 1.0)
+    tflops = flops / t / 1e12
+    out = {"N": N, "H": H, "V": V, "K": K, "T": T, "chunk": chunk, "steps": steps,
+           "tokens_per_s": N / t, "ms_per_step": t * 1e3, "tflops": tflops,
+           "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
+           "peak_gib": peak,
+           "inputs_gib": sum(workloads.bytes_of_inputs(cfg).values()) / 2**30,
+           "grads_gib": 4 * (N * H + V * H) / 2**30,
+           "workspace_gib": ws_bytes / 2**30,
+           "dense_fp32_logits_gib": 4 * N * V / 2**30, "loss": loss, "clocks": clk}
+    del inp, gh, gW, ws, h_, W_, i_, l_
+    return out
+
+
 def run_sweep(args):
     import dataclasses
 
@@ -563,6 +626,7 @@ def run_sweep(args):
     kd.lib()
     peaks, _ = load_peaks()
     oracle_rate = {}   # per workload: the float64 oracle on its first tokens (host cores)
+    flags = kd.KD_FLAG_MIN_SCRATCH if args.min_scratch else 0
     for name, n_tokens, chunk in SWEEP_POINTS:
         cfg = workloads.CONFIGS[name]
         if name not in oracle_rate and not args.skip_cpu_baseline:
@@ -575,56 +639,44 @@ def run_sweep(args):
         if n_tokens:
             cfg = dataclasses.replace(cfg, N=n_tokens, name=f"{name}_n{n_tokens}")
         chunk = chunk or cfg.chunk
-        N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
-        torch.cuda.synchronize(dev)
-        torch.cuda.empty_cache()
-        mem0 = torch.cuda.memory_allocated(dev)
-        inp = workloads.make_inputs(cfg, seed=0, device=dev)
-        torch.cuda.synchronize(dev)
-        torch.cuda.reset_peak_memory_stats(dev)     # not the input draw's temporaries
-        gh = torch.empty((N, H), dtype=torch.float32, device=dev)
-        gW = torch.empty((V, H), dtype=torch.float32, device=dev)
-        flags = kd.KD_FLAG_MIN_SCRATCH if args.min_scratch else 0
-        ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, chunk, flags),
-                         dtype=torch.uint8, device=dev)
-        h_, W_, i_, l_ = inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"]
-
-        def call():
-            return kd.kd_topk_kl_fwd_bwd_flags(h_, W_, i_, l_, None, T, chunk, flags, gh, gW, ws)
-        loss = call()
-        torch.cuda.synchronize(dev)
-        peak = (torch.cuda.max_memory_allocated(dev) - mem0) / 2**30
-        # time one more warm call, then enough steps for ~1.5 s of samples
-        w0 = time.perf_counter()
-        call()
-        steps = max(3, min(200, int(1.5 / max(time.perf_counter() - w0, 1e-4)) + 1))
-        clocks = ClockSampler(_gpu_id(0))
-        clocks.start()
-        time.sleep(0.2)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            loss = call()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        clk = clocks.stop()
-        t = e0.elapsed_time(e1) / 1e3 / steps
-        tflops = cfg.flops / t / 1e12
+        point = _sweep_point(kd, cfg, chunk, flags, dev, peaks)
         print(json.dumps({
             "sweep": "memory_and_throughput", "workload": cfg.name,
             "grad_W_depth": "one chunk (minimal scratch)" if args.min_scratch else "two chunks",
-            "N": N, "H": H, "V": V,
-            "K": K, "T": T, "chunk": chunk, "steps": steps, "tokens_per_s": N / t,
-            "ms_per_step": t * 1e3, "tflops": tflops,
-            "frac_bf16_peak_burst": tflops / float(peaks["bf16_tflops"]),
-            "peak_gib": peak,
-            "inputs_gib": sum(workloads.bytes_of_inputs(cfg).values()) / 2**30,
-            "grads_gib": 4 * (N * H + V * H) / 2**30,
-            "workspace_gib": ws.numel() / 2**30,
-            "dense_fp32_logits_gib": 4 * N * V / 2**30, "loss": loss,
-            "clocks": clk, "cpu_baseline": oracle_rate.get(name)}), flush=True)
-        del inp, gh, gW, ws, h_, W_, i_, l_
+            **point, "cpu_baseline": oracle_rate.get(name)}), flush=True)
+
+
+# The full logits grid against the chunked plan (glonce.com, body: the
+# "forward-chunked" variant keeps the teacher sparse but holds the student's
+# whole [tokens x vocab] logits for the backward pass).  The same library
+# holds exactly that grid when the stored-logits backward runs as one chunk
+# of all N tokens: fp32 z [N, V] and bf16 dZ [N, V].  Both plans on the
+# gptoss32k head at growing N; a point that would not fit is reported as
+# skipped with what it needed.
+GRID_TOKENS = (8192, 16384, 32768, 65536, 131072, 262144)
+
+
+def run_sweep_grid(args):
+    import dataclasses
+
+    import torch
+
+    import chunked_top_kl_gemm_b300 as kd
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kd.lib()
+    peaks, _ = load_peaks()
+    base = workloads.CONFIGS["gptoss32k"]
+    for n in GRID_TOKENS:
+        cfg = dataclasses.replace(base, N=n, name=f"gptoss32k_n{n}")
+        for plan, chunk, flags in (("chunked (recompute, chunk 2048)", base.chunk, 0),
+                                   ("full logits grid (stored logits, one chunk of N)", n,
+                                    kd.KD_FLAG_STORE_LOGITS)):
+            point = _sweep_point(kd, cfg, chunk, flags, dev, peaks)
+            print(json.dumps({"sweep": "full_grid_vs_chunked", "workload": cfg.name,
+                              "plan": plan, **point}), flush=True)
 
 
 # ------------------------------------------------------------------ cache builder
@@ -716,6 +768,9 @@ def main(argv=None):
                     help="one chunk's dZ in the workspace: grad_W formed per chunk")
     ap.add_argument("--allow-short-warmup", action="store_true",
                     help="profiling runs only: honour --warmup below 3")
+    ap.add_argument("--sweep-grid", action="store_true",
+                    help="peak memory and throughput of the full logits grid (stored logits, one "
+                         "chunk of all tokens) against the chunked plan, gptoss32k head, 8K-256K")
     ap.add_argument("--sweep", action="store_true",
                     help="peak memory and throughput over token counts and chunk sizes "
                          "(one JSON line per point)")
@@ -724,6 +779,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.sweep:
         return run_sweep(args)
+    if args.sweep_grid:
+        return run_sweep_grid(args)
     if args.cache_build:
         return run_cache_build(args)
     if args.impl == "reference":

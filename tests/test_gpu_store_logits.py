@@ -108,6 +108,34 @@ def test_chunk_of_more_than_65535_rows():
     assert rel_l2(b[1].cpu().numpy()[rows], want["grad_hidden"]) <= GRAD_REL_L2
 
 
+def test_full_logits_grid_past_int32_elements():
+    """One chunk of all N tokens with stored logits holds the whole [N, V]
+    grid: 12,288 x 200,704 = 2.47e9 elements, past what a 32-bit element
+    offset reaches.  Bitwise equal to the recompute at the same chunk; the
+    loss bitwise equal to the 2048-row chunked plan (its per-token terms do
+    not depend on the chunking) and the gradients equal up to fp32
+    summation order; grad_hidden rows against the oracle."""
+    ensure_lib()
+    cfg = workloads.custom("z_grid", N=12288, H=64, V=200704, K=16, T=1.0, chunk=12288,
+                           hidden_rms_norm=True, teacher="zipf")
+    assert cfg.N * cfg.V > 2**31
+    inp_cpu = workloads.make_inputs(cfg, seed=17)
+    inp = to_device(inp_cpu)
+    b = _run(inp, cfg.T, cfg.N, kd.KD_FLAG_STORE_LOGITS)
+    a = _run(inp, cfg.T, cfg.N, 0)
+    assert a[0] == b[0]
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    del a
+    c = _run(inp, cfg.T, 2048, 0)
+    assert c[0] == b[0]
+    assert rel_l2(b[1].cpu().numpy(), c[1].cpu().numpy()) <= 1e-4
+    assert rel_l2(b[2].cpu().numpy(), c[2].cpu().numpy()) <= 1e-4
+    rows = np.array([0, 1, 6143, 6144, 10922, 12286, 12287])
+    want = oracle.rows_forward(inp_cpu["hidden"][rows], inp_cpu["W"], inp_cpu["topk_idx"][rows],
+                               inp_cpu["topk_logit"][rows], cfg.T, N_total=cfg.N)
+    assert rel_l2(b[1].cpu().numpy()[rows], want["grad_hidden"]) <= GRAD_REL_L2
+
+
 def test_workspace_grows_by_the_chunk_logits():
     ensure_lib()
     N, H, V, K, chunk = 32768, 2880, 201088, 100, 2048
