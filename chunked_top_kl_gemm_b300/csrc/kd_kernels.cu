@@ -306,15 +306,19 @@ cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N
 // One block per 8 chunk rows (32 warps).  Lane l of warp w takes row
 // r0 + (l & 7) and the vocab tiles t = p + 4 (w + 32 i), p = l >> 3: it
 // combines their (max, sum) partials (log2 units) in fp32 relative to its
-// running max, a warp load covering 4 tiles x 8 consecutive rows.  Warp
-// w < 8 then merges row r0 + w's 128 partial pairs in double into
-// lse2 = log2 sum_v 2^(z_v log2e / T), and folds the row's KL term
+// running max, a warp load covering 4 tiles x 8 consecutive rows; a lane's
+// loads are issued LSE_BATCH at a time before any is folded.  Warp w < 8
+// then merges row r0 + w's 128 partial pairs into
+// lse2 = log2 sum_v 2^(z_v log2e / T) and forms the row's KL term
 // sum_k p_k (log p_k - z_k/T + lse),  lse = lse2 ln 2,  with the lanes
-// striding over the K cached entries.
+// striding over the K cached entries.  The merges and the dot product run in
+// fp32 with a fixed butterfly order (fp64 is a small fraction of fp32's rate
+// on this part); only the last combination of the row's terms is in double.
 constexpr int LSE_ROWS = 8;
 constexpr int LSE_PHASES = 4;     // lanes per row in a warp
 constexpr int LSE_WARPS = 32;
 constexpr int LSE_SLOTS = LSE_WARPS * LSE_PHASES;   // partial pairs per row
+constexpr int LSE_BATCH = 8;      // partial loads a lane has in flight
 
 __device__ __forceinline__ void lse_fold(float& M, float& S, float2 v) {
   const float m_new = fmaxf(M, v.x);
@@ -338,14 +342,18 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
   if (r < rows_valid) {
     const float2* col = part + r;
     constexpr int STEP = LSE_PHASES * LSE_WARPS;
-    int t = ph + LSE_PHASES * warp;
-    for (; t + STEP < n_tiles; t += 2 * STEP) {
-      const float2 a = col[static_cast<long long>(t) * c_alloc];
-      const float2 b = col[static_cast<long long>(t + STEP) * c_alloc];
-      lse_fold(M, S, a);
-      lse_fold(M, S, b);
+    for (int t0 = ph + LSE_PHASES * warp; t0 < n_tiles; t0 += LSE_BATCH * STEP) {
+      float2 v[LSE_BATCH];
+#pragma unroll
+      for (int i = 0; i < LSE_BATCH; ++i) {
+        const int t = t0 + i * STEP;
+        v[i] = t < n_tiles ? col[static_cast<long long>(t) * c_alloc]
+                           : make_float2(-CUDART_INF_F, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < LSE_BATCH; ++i)
+        if (t0 + i * STEP < n_tiles) lse_fold(M, S, v[i]);
     }
-    if (t < n_tiles) lse_fold(M, S, col[static_cast<long long>(t) * c_alloc]);
   }
   const int slot = warp * LSE_PHASES + ph;
   sM[rr][slot] = M;
@@ -365,27 +373,27 @@ __global__ void __launch_bounds__(LSE_WARPS * 32) kd_lse_loss(
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Mr = fmaxf(Mr, __shfl_xor_sync(0xffffffffu, Mr, o));
-  double Sr = 0.0;
+  float Sr = 0.f;
 #pragma unroll
   for (int i = 0; i < LSE_SLOTS / 32; ++i)
-    if (s4[i] > 0.f) Sr += static_cast<double>(s4[i]) * static_cast<double>(exp2f(m4[i] - Mr));
+    if (s4[i] > 0.f) Sr = fmaf(s4[i], exp2f(m4[i] - Mr), Sr);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Sr += __shfl_xor_sync(0xffffffffu, Sr, o);
-  const double lse2 = static_cast<double>(Mr) + log2(Sr);
-  const double lse = lse2 * 0.69314718055994530942;  // ln 2
+  const float lse2 = Mr + log2f(Sr);
   const long long g = static_cast<long long>(grow0) + row;
-  double dot = 0.0;
+  float dot = 0.f;
   for (int j = lane; j < K; j += 32) {
     const float z = zg[static_cast<long long>(row) * K + j];
-    dot += static_cast<double>(sp[g * K + j]) * static_cast<double>(z);
+    dot = fmaf(sp[g * K + j], z, dot);
     if (dbg_zg) dbg_zg[g * K + perm[g * K + j]] = z;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
   if (lane == 0) {
-    lse2_out[row] = static_cast<float>(lse2);
+    const double lse = static_cast<double>(lse2) * 0.69314718055994530942;  // ln 2
+    lse2_out[row] = lse2;
     const bool live = !mask || mask[g] != 0;
-    loss_rows[g] = live ? ent[g] + lse * psum[g] - dot * invT : 0.0;
+    loss_rows[g] = live ? ent[g] + lse * psum[g] - static_cast<double>(dot) * invT : 0.0;
     if (dbg_lse) dbg_lse[g] = static_cast<float>(lse);
   }
 }

@@ -26,8 +26,9 @@
  * up in dZ and give one loss term each.
  *
  * Arithmetic.  hidden and W are bf16; the GEMMs run on tcgen05 tensor cores
- * with fp32 accumulation; the per-token loss terms and their sum are
- * accumulated in double; dZ is held as bf16 scratch for two consecutive
+ * with fp32 accumulation; each token's logsumexp and dot product with the
+ * teacher are fp32, its loss term is combined and the terms summed in
+ * double; dZ is held as bf16 scratch for two consecutive
  * chunks (2 x chunk x V; one chunk with KD_FLAG_MIN_SCRATCH); grad_W is
  * accumulated over those chunk pairs in fp32 in device memory.
  *
