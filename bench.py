@@ -12,9 +12,9 @@ GPT-OSS-like head at 32,768 tokens (H=2880, V=201,088, K=100, chunk 2048),
 the configuration the pages' 32K figures and GPT-OSS 20B run refer to.
 
 Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
-independent replica of the workload (the loss has no cross-GPU exchange in
-this build), the timed region is bracketed by barriers and the time is the
-maximum over ranks.
+independent replica of the workload (the library has no cross-GPU exchange),
+the timed region is bracketed by barriers and the time is the maximum over
+ranks.
 """
 from __future__ import annotations
 
@@ -646,11 +646,11 @@ def run_sweep(args):
             **point, "cpu_baseline": oracle_rate.get(name)}), flush=True)
 
 
-# The full logits grid against the chunked plan (glonce.com, body: the
-# "forward-chunked" variant keeps the teacher sparse but holds the student's
-# whole [tokens x vocab] logits for the backward pass).  The same library
-# holds exactly that grid when the stored-logits backward runs as one chunk
-# of all N tokens: fp32 z [N, V] and bf16 dZ [N, V].  Both plans on the
+# The full logits grid against the chunked plan.  The pages' "forward-chunked"
+# comparison variant uses the sparse teacher cache but holds every student
+# logit of the batch for its backward pass (glonce.com, body).  The same
+# library holds exactly that grid when the stored-logits backward runs as one
+# chunk of all N tokens: fp32 z [N, V] and bf16 dZ [N, V].  Both plans on the
 # gptoss32k head at growing N; a point that would not fit is reported as
 # skipped with what it needed.
 GRID_TOKENS = (8192, 16384, 32768, 65536, 131072, 262144)

@@ -3,9 +3,9 @@
 // The method (Multiverse Computing, "Efficient Knowledge Distillation for
 // LLMs: Offline Top-K Logits and a Fused Chunked KL Loss", as summarised on
 // glonce.com, body, and ainewsbank.com, "Two changes remove different
-// bottlenecks"): per token chunk, project hidden states to logits, fold the
-// chunk into the running loss and discard it; in the backward pass recompute
-// each chunk's logits instead of storing them.  The teacher side is an offline
+// bottlenecks"): a token chunk's logits are formed, reduced into the running
+// loss and dropped, and the backward pass forms them again rather than
+// keeping them.  The teacher side is an offline
 // cache of the K highest teacher logits and their ids per token (epoka.news,
 // "The two proposed changes").
 //

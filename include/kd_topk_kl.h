@@ -9,12 +9,11 @@
  *     offline, and stored per position (epoka.news, "The two proposed
  *     changes"; ainewsbank.com, "Two changes remove different bottlenecks":
  *     K = 100 there);
- *   - the loss projects hidden states to logits one sequence chunk at a
- *     time, folds each chunk into the running loss and discards it, and
- *     recomputes the chunks during the backward pass instead of storing them
- *     (glonce.com, body, the paragraph on Multiverse's fix), so the
- *     [tokens x vocab] logit matrix is never materialised (glonce.com,
- *     "Key facts").
+ *   - the loss handles the token positions chunk by chunk: a chunk's
+ *     logits are formed, reduced into the running loss and dropped, then
+ *     formed again during the backward pass rather than kept (glonce.com,
+ *     body, the paragraph on Multiverse's fix), so no [tokens x vocab]
+ *     logit matrix ever exists in memory (glonce.com, "Key facts").
  * The pages do not print the formula.  This library computes the standard
  * truncated-teacher KL, with z_n = W h_n (no bias), T > 0:
  *   p_nk    = softmax_k(topk_logit_n / T)              over the K entries

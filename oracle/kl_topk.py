@@ -9,13 +9,14 @@ The pages describe the method but do not print its formula:
 
 * offline top-K caching keeps, per token position, the teacher's K highest
   logits and their token ids (epoka.news, "The two proposed changes";
-  ainewsbank.com, "Two changes remove different bottlenecks": "the 100 most
-  likely token scores at every position");
-* the fused chunked loss projects hidden states to logits one sequence chunk
-  at a time, folds each chunk into the running loss and discards it, and
-  recomputes the chunks in the backward pass (glonce.com, body, the
-  paragraph on Multiverse's fix); chunking preserves the calculation
-  (ainewsbank.com, "Two changes remove different bottlenecks").
+  ainewsbank.com, "Two changes remove different bottlenecks", which puts K
+  at 100);
+* the fused chunked loss works through the token positions chunk by chunk:
+  a chunk's logits are formed, reduced into the running loss and dropped,
+  then formed again for the gradients rather than kept (glonce.com, body,
+  the paragraph on Multiverse's fix); the chunked form computes the same
+  numbers as the plain one (ainewsbank.com, "Two changes remove different
+  bottlenecks").
 
 Because chunking and recomputation leave the result unchanged, this oracle
 is the plain dense definition, with one row block at a time only to bound
