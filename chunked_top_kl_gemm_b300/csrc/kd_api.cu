@@ -146,6 +146,7 @@ uint32_t b_box_rows(int variant) {
 
 // ---------------------------------------------------------------- plan
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+constexpr long long kMaxChunk = 1LL << 30;   // rows of one chunk at most
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Plan {
@@ -203,6 +204,7 @@ Plan make_plan(long long N, int H, int V, int K, int chunk, int sms, bool store_
   long long c = cdiv(chunk, 128) * 128;
   const long long cmax = cdiv(N, 128) * 128;
   if (c > cmax) c = cmax;
+  if (c > kMaxChunk) c = kMaxChunk;   // row coordinates of the chunk buffers stay in int
   p.chunk = static_cast<int>(c);
   p.n_chunks = static_cast<int>(cdiv(N, c));
   p.gg = (min_scratch || p.n_chunks < 2) ? 1 : 2;
@@ -676,6 +678,7 @@ CachePlan make_cache_plan(long long N, int V, int chunk) {
   long long c = cdiv(chunk, 128) * 128;
   const long long cmax = cdiv(N, 128) * 128;
   if (c > cmax) c = cmax;
+  if (c > kMaxChunk) c = kMaxChunk;   // row coordinates of the chunk buffers stay in int
   p.chunk = static_cast<int>(c);
   p.n_chunks = static_cast<int>(cdiv(N, c));
   p.vt = static_cast<int>(cdiv(V, kd::gemm_bn(kd::GV_FWDZ)));

@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "kd_gemm.cuh"
 #include "kd_internal.h"
 
@@ -68,13 +70,18 @@ using CfgTestKK2S = GemmCfg<256, false, false, 3, EPI_F32, true, 2>;
 template <class C>
 static int resident_units() {
   constexpr int kMaxDev = 64;
-  static int cached[kMaxDev] = {};
+  // host threads may query at once: relaxed atomics (every writer stores
+  // the same value)
+  static std::atomic<int> cached[kMaxDev];
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     dev = -1;
   }
-  if (dev >= 0 && dev < kMaxDev && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < kMaxDev) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   if (dev >= 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     sms = 148;
@@ -105,22 +112,22 @@ static int resident_units() {
     else
       cudaGetLastError();
   }
-  if (dev >= 0 && dev < kMaxDev) cached[dev] = width;
+  if (dev >= 0 && dev < kMaxDev) cached[dev].store(width, std::memory_order_relaxed);
   return width;
 }
 
 template <class C>
 static cudaError_t launch_cfg(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                               const GemmArgs& g, const EpiArgs& e, cudaStream_t s) {
-  static bool attr_set[64] = {};  // per instantiation and device
+  static std::atomic<bool> attr_set[64];  // per instantiation and device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
     err = cudaFuncSetAttribute(kd_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   const long long units = static_cast<long long>(g.m_tiles) * g.n_tiles * g.splits;
   if (units <= 0) return cudaSuccess;
@@ -286,14 +293,14 @@ cudaError_t launch_prep_topk(const int32_t* idx, const float* logit, long long N
   int wpb = 65536 / (P * 8);
   wpb = wpb < 1 ? 1 : (wpb > 8 ? 8 : wpb);
   const size_t smem = static_cast<size_t>(wpb) * P * 8;
-  static bool attr_set[64] = {};  // per device
+  static std::atomic<bool> attr_set[64];  // per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(kd_prep_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   const long long blocks = (N + wpb - 1) / wpb;
   kd_prep_topk<<<static_cast<unsigned>(blocks), wpb * 32, smem, s>>>(
@@ -805,15 +812,15 @@ cudaError_t launch_topk_select(const float* z, int V, const float2* part, int n_
                                uint32_t* cnt, unsigned long long* cand, int32_t* out_idx,
                                float* out_val, cudaStream_t s) {
   const size_t smem = SEL_CAP * sizeof(unsigned long long) + (SEL_BINS + SEL_THREADS) * 4;
-  static bool attr_set[64] = {};  // per device
+  static std::atomic<bool> attr_set[64];  // per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(kd_sel_exact, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   constexpr int rows_per_block = SEL_TAU_THREADS / 32;
   kd_sel_tau<<<(rows_valid + rows_per_block - 1) / rows_per_block, SEL_TAU_THREADS, 0, s>>>(

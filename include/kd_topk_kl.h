@@ -90,9 +90,9 @@ typedef enum kd_status {
  *   K           cached entries per token, 1 <= K <= min(V, 8192)
  *   T           temperature, finite and > 0
  *   chunk       token rows per chunk (>= 1); rounded up to a multiple of 128
- *               and capped at N rounded up likewise.  Scratch grows as
- *               2 x chunk x V x 2 bytes (the bf16 dZ of two chunks; one
- *               chunk's when N fits in one chunk).
+ *               and capped at N rounded up likewise, and at 2^30 rows.
+ *               Scratch grows as 2 x chunk x V x 2 bytes (the bf16 dZ of
+ *               two chunks; one chunk's when N fits in one chunk).
  *   loss        HOST float*: the mean over the N tokens
  *   grad_hidden fp32 [N, H] (device), overwritten
  *   grad_W      fp32 [V, H] (device), overwritten
