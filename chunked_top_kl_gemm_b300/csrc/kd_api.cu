@@ -1,5 +1,6 @@
 // C ABI of the fused chunked top-K KL loss: argument validation, workspace
 // plan, TMA descriptors and the chunk loop (all launches on one stream).
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -46,7 +47,7 @@ const char* const kProfNames[PK_COUNT] = {"prep_topk", "gemm_fwd_lse_gather", "l
 
 struct Profiler {
   std::mutex mu;
-  bool on = false;
+  std::atomic<bool> on{false};   // read by every call, profiling or not
   double total_ms[PK_COUNT] = {};
   long long launches[PK_COUNT] = {};
   // events of the call in flight (reused across calls)
@@ -61,6 +62,13 @@ Profiler& prof() {
 // Set while an asynchronous call enqueues: its launches are not timed (the
 // events could only be read after a synchronisation the call does not do).
 thread_local bool t_prof_off = false;
+
+// A call starts with no event pairs in flight (touched only while profiling,
+// which is documented as single-threaded).
+void prof_reset_call() {
+  Profiler& P = prof();
+  if (P.on.load(std::memory_order_relaxed) && !t_prof_off) P.used = 0;
+}
 
 // Bracket one launch.  Returns the index of its event pair or -1.
 struct ProfScope {
@@ -299,7 +307,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   }
   const Plan p = make_plan(N, H, V, K, chunk, device_sms(), store_z, min_scratch);
   if (!ws || ws_bytes < p.total) return KD_ERR_OOM;
-  prof().used = 0;
+  prof_reset_call();
   if (!aligned(ws, 256)) return KD_ERR_ALIGNMENT;
   if (!is_device_ptr(ws)) return KD_ERR_INVALID_ARG;
 
@@ -713,7 +721,7 @@ kd_status cache_build_impl(const void* hidden, const void* W, int64_t N, int H, 
   const CachePlan p = make_cache_plan(N, V, chunk);
   if (workspace_bytes < p.total) return KD_ERR_OOM;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  prof().used = 0;
+  prof_reset_call();
   uint8_t* base = static_cast<uint8_t*>(workspace);
   DevStatus* dst = reinterpret_cast<DevStatus*>(base + p.off_status);
   float2* part = reinterpret_cast<float2*>(base + p.off_part);
