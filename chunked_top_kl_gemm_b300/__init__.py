@@ -194,11 +194,40 @@ def _check_inputs(hidden, W, topk_idx, topk_logit):
             raise ValueError(f"{name} must be a CUDA tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
+        if t.device != hidden.device:
+            raise ValueError(f"{name} must be on {hidden.device}")
     N, H = hidden.shape
     V, H2 = W.shape
     if H2 != H or topk_idx.shape != topk_logit.shape or topk_idx.shape[0] != N:
         raise ValueError("shape mismatch: hidden [N,H], W [V,H], topk_* [N,K]")
     return N, H, V, topk_idx.shape[1]
+
+
+def _check_out(name, t, shape, dtype, device):
+    """A buffer the library writes: the library sees only its address, so its
+    dtype, shape, layout and device are checked here (a smaller buffer would
+    be written past its end)."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor of shape {tuple(shape)}")
+
+
+def _check_grads(grad_hidden, grad_W, hidden, V):
+    import torch
+    N, H = hidden.shape
+    _check_out("grad_hidden", grad_hidden, (N, H), torch.float32, hidden.device)
+    _check_out("grad_W", grad_W, (V, H), torch.float32, hidden.device)
+
+
+def _check_workspace(workspace, hidden):
+    if workspace is None or not workspace.is_cuda or workspace.device != hidden.device \
+            or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {hidden.device}")
 
 
 def kd_topk_kl_workspace_size(N: int, H: int, V: int, K: int, chunk: int) -> int:
@@ -212,6 +241,7 @@ def kd_topk_kl_fwd_bwd(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
     Writes grad_hidden / grad_W in place and returns the loss.
     """
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    _check_grads(grad_hidden, grad_W, hidden, V)
     loss = ctypes.c_float(0.0)
     with _on_device(hidden):
         st = lib().kd_topk_kl_fwd_bwd(_ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit),
@@ -225,6 +255,8 @@ def kd_topk_kl_fwd_bwd_ex(hidden, W, topk_idx, topk_logit, T: float, chunk: int,
                           grad_hidden, grad_W, workspace, stream=None) -> float:
     """Caller stream (default: torch's current stream) and workspace tensor."""
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    _check_grads(grad_hidden, grad_W, hidden, V)
+    _check_workspace(workspace, hidden)
     loss = ctypes.c_float(0.0)
     with _on_device(hidden):
         st = lib().kd_topk_kl_fwd_bwd_ex(
@@ -254,6 +286,10 @@ def kd_topk_kl_fwd_bwd_masked(hidden, W, topk_idx, topk_logit, token_mask, T: fl
     import torch
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     token_mask = _check_mask(token_mask, N)
+    _check_grads(grad_hidden, grad_W, hidden, V)
+    _check_workspace(workspace, hidden)
+    if token_mask is not None and token_mask.device != hidden.device:
+        raise ValueError(f"token_mask must be on {hidden.device}")
     loss = ctypes.c_float(0.0)
     with _on_device(hidden):
         st = lib().kd_topk_kl_fwd_bwd_masked(
@@ -275,6 +311,10 @@ def kd_topk_kl_fwd_bwd_flags(hidden, W, topk_idx, topk_logit, token_mask, T: flo
     """Mask (or None) and KD_FLAG_* flags (accumulate, store logits)."""
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     token_mask = _check_mask(token_mask, N)
+    _check_grads(grad_hidden, grad_W, hidden, V)
+    _check_workspace(workspace, hidden)
+    if token_mask is not None and token_mask.device != hidden.device:
+        raise ValueError(f"token_mask must be on {hidden.device}")
     loss = ctypes.c_float(0.0)
     with _on_device(hidden):
         st = lib().kd_topk_kl_fwd_bwd_flags(
@@ -295,6 +335,10 @@ def kd_topk_kl_fwd_bwd_sharded(hidden, W, topk_idx, topk_logit, token_mask, T: f
     adds into grad_W on one device)."""
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     token_mask = _check_mask(token_mask, N)
+    _check_grads(grad_hidden, grad_W, hidden, V)
+    _check_workspace(workspace, hidden)
+    if token_mask is not None and token_mask.device != hidden.device:
+        raise ValueError(f"token_mask must be on {hidden.device}")
     loss = ctypes.c_float(0.0)
     with _on_device(hidden):
         st = lib().kd_topk_kl_fwd_bwd_sharded(
@@ -316,9 +360,14 @@ def kd_topk_kl_fwd_bwd_async(hidden, W, topk_idx, topk_logit, token_mask, T: flo
     import torch
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
     token_mask = _check_mask(token_mask, N)
+    _check_grads(grad_hidden, grad_W, hidden, V)
+    _check_workspace(workspace, hidden)
+    if token_mask is not None and token_mask.device != hidden.device:
+        raise ValueError(f"token_mask must be on {hidden.device}")
     for name, t, dt in (("loss_out", loss_out, torch.float32), ("status_out", status_out, torch.int32)):
-        if t.dtype != dt or t.numel() < 1 or not t.is_cuda:
-            raise ValueError(f"{name} must be a {dt} CUDA tensor with at least one element")
+        if t.dtype != dt or t.numel() < 1 or not t.is_cuda or t.device != hidden.device:
+            raise ValueError(f"{name} must be a {dt} CUDA tensor on {hidden.device} with at "
+                             "least one element")
     with _on_device(hidden):
         st = lib().kd_topk_kl_fwd_bwd_async(
             _ptr(hidden), _ptr(W), _ptr(topk_idx), _ptr(topk_logit), _ptr(token_mask), N, H, V, K,
@@ -350,15 +399,20 @@ def kd_topk_cache_build(hidden, W, K: int, chunk: int = 2048, *, topk_idx=None,
     N, H = hidden.shape
     V = W.shape[0]
     dev = hidden.device
+    if W.shape[1] != H or W.device != dev:
+        raise ValueError("W must be [V, H] on hidden's device")
     if topk_idx is None:
         topk_idx = torch.empty((N, K), dtype=torch.int32, device=dev)
     if topk_logit is None:
         topk_logit = torch.empty((N, K), dtype=torch.float32, device=dev)
+    _check_out("topk_idx", topk_idx, (N, K), torch.int32, dev)
+    _check_out("topk_logit", topk_logit, (N, K), torch.float32, dev)
     if workspace is None:
         nbytes = kd_topk_cache_workspace_size(N, H, V, K, chunk)
         if nbytes == 0:
             raise KdError(1, "kd_topk_cache_workspace_size")
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _check_workspace(workspace, hidden)
     with _on_device(hidden):
         st = lib().kd_topk_cache_build(_ptr(hidden), _ptr(W), N, H, V, int(K), int(chunk),
                                        _ptr(topk_idx), _ptr(topk_logit), _ptr(workspace),
@@ -374,7 +428,15 @@ def kd_topk_kl_debug(hidden, W, topk_idx, topk_logit, T: float, chunk: int, grad
     """``kd_topk_kl_fwd_bwd_ex`` plus the debug exports (fp32 ``lse`` [N], fp32 ``zg``
     [N,K], int32 ``found_idx`` [N,K] pre-filled by the caller, float64 ``loss_rows`` [N])
     and the bounded-wait test hook."""
+    import torch
     N, H, V, K = _check_inputs(hidden, W, topk_idx, topk_logit)
+    _check_grads(grad_hidden, grad_W, hidden, V)
+    _check_workspace(workspace, hidden)
+    for name, t, shape, dt in (("lse", lse, (N,), torch.float32), ("zg", zg, (N, K), torch.float32),
+                               ("found_idx", found_idx, (N, K), torch.int32),
+                               ("loss_rows", loss_rows, (N,), torch.float64)):
+        if t is not None:
+            _check_out(name, t, shape, dt, hidden.device)
     # inject_timeout: False / True (= 1, the forward GEMM) or 1..4 (forward,
     # recompute, grad_hidden, grad_W GEMM of the first chunk)
     opts = _DebugOpts(_ptr(lse) or None, _ptr(zg) or None, _ptr(found_idx) or None,

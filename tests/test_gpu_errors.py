@@ -99,3 +99,27 @@ def test_small_workspace_is_oom_status():
         kd.kd_topk_kl_fwd_bwd_ex(inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"],
                                  CFG.T, CFG.chunk, gh, gW, ws)
     assert ei.value.name == "KD_ERR_OOM"
+
+
+def test_binding_checks_the_buffers_the_library_writes():
+    # the library sees only addresses: a gradient buffer of the wrong dtype,
+    # shape or layout, or on the host, is refused before anything is launched
+    inp = _inputs()
+    N, H = inp["hidden"].shape
+    V = inp["W"].shape[0]
+    ws = kd.alloc_workspace(CFG.N, CFG.H, CFG.V, CFG.K, CFG.chunk, device="cuda")
+    gh = torch.empty((N, H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+    args = (inp["hidden"], inp["W"], inp["topk_idx"], inp["topk_logit"], CFG.T, CFG.chunk)
+    with pytest.raises(TypeError):
+        kd.kd_topk_kl_fwd_bwd_ex(*args, gh.to(torch.bfloat16), gW, ws)
+    with pytest.raises(ValueError):
+        kd.kd_topk_kl_fwd_bwd_ex(*args, gh, gW[:-8], ws)
+    with pytest.raises(ValueError):
+        kd.kd_topk_kl_fwd_bwd_ex(*args, torch.empty((H, N), device="cuda").t(), gW, ws)
+    with pytest.raises(ValueError):
+        kd.kd_topk_kl_fwd_bwd_ex(*args, gh, gW.cpu(), ws)
+    with pytest.raises(ValueError):
+        kd.kd_topk_kl_fwd_bwd_flags(*args[:4], None, CFG.T, CFG.chunk, 0, gh, gW, ws.cpu())
+    loss = kd.kd_topk_kl_fwd_bwd_ex(*args, gh, gW, ws)   # the same call with good buffers
+    assert np.isfinite(loss)
