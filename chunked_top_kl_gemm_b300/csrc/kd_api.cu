@@ -130,12 +130,52 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// The tensor-map encoder is a driver-API call and needs a context current on
+// the calling thread; a thread that has made no context-binding runtime call
+// yet has none (a new host thread).  Every entry point therefore binds the
+// current device's primary context before encoding, unless the thread
+// already has a context current (a caller's own context is left alone).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+bool bind_current_device() {
+  CtxGetCurrentFn get = ctx_get_current_fn();
+  CUcontext cur = nullptr;
+  if (get && get(&cur) == CUDA_SUCCESS && cur != nullptr) return true;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "could not make the current device's context current");
+    return false;
+  }
+  return true;
+}
+
 // 2-D row-major tensor [outer][inner], 128-byte swizzled boxes of
-// box_inner x box_outer elements.
+// box_inner x box_outer elements.  On failure the driver's result code is
+// left in the thread's last-error text.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
               uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
+  if (!fn) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled: no driver entry point");
+    return false;
+  }
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
   cuuint32_t box[2] = {box_inner, box_outer};
@@ -143,7 +183,12 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* bas
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return false;
+  }
+  return true;
 }
 
 // Rows of the B operand's TMA box of a GEMM variant (K-major B): the rows one
@@ -336,6 +381,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   CUtensorMap tm_hid_k, tm_w_k, tm_dz_st, tm_dz_k256, tm_w_mn, tm_k4_st, tm_dz_mn, tm_hid_mn, tm_gw;
+  if (!bind_current_device()) return KD_ERR_CUDA;
   bool ok = true;
   ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
   ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, b_box_rows(kd::GV_FWD));
@@ -349,10 +395,7 @@ kd_status run_impl(const void* hidden, const void* W, const int32_t* idx, const 
   ok &= make_map(&tm_gw, F32, 4, gW, H, V, 32, 32);
   CUtensorMap tm_z_st;
   if (store_z) ok &= make_map(&tm_z_st, F32, 4, zbuf, V, p.chunk, 32, 32);
-  if (!ok) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed");
-    return KD_ERR_CUDA;
-  }
+  if (!ok) return KD_ERR_CUDA;   // make_map left the driver's result in the last-error text
 
   const bool sharded = n_norm > 0.0;
   const float scale2 = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
@@ -646,6 +689,7 @@ kd_status kd_gemm_bf16_test(const void* A, const void* B, float* C, int M, int N
   }
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap ta, tb, tc;
+  if (!bind_current_device()) return KD_ERR_CUDA;
   bool ok = true;
   ok &= a_mn ? make_map(&ta, BF16, 2, A, M, K, 64, 64) : make_map(&ta, BF16, 2, A, K, M, 64, 128);
   ok &= b_mn ? make_map(&tb, BF16, 2, B, N, K, 64, 64)
@@ -732,14 +776,12 @@ kd_status cache_build_impl(const void* hidden, const void* W, int64_t N, int H, 
 
   const auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tm_hid_k, tm_w_k, tm_z_st;
+  if (!bind_current_device()) return KD_ERR_CUDA;
   bool ok = true;
   ok &= make_map(&tm_hid_k, BF16, 2, hidden, H, N, 64, 128);
   ok &= make_map(&tm_w_k, BF16, 2, W, H, V, 64, b_box_rows(kd::GV_FWDZ));
   ok &= make_map(&tm_z_st, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, zbuf, V, p.chunk, 32, 32);
-  if (!ok) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed");
-    return KD_ERR_CUDA;
-  }
+  if (!ok) return KD_ERR_CUDA;   // make_map left the driver's result in the last-error text
   KD_CUDA(cudaMemsetAsync(dst, 0, sizeof(DevStatus), s));
   for (int j = 0; j < p.n_chunks; ++j) {
     const int row0 = j * p.chunk;

@@ -50,8 +50,13 @@
  * outputs.  kd_topk_kl_fwd_bwd_async leaves the loss and the device-side
  * status in device memory and does not wait (see there).
  *
- * Thread safety.  Calls on different streams may run concurrently if they
- * use different workspaces.
+ * Thread safety.  Calls on different streams may run concurrently, from one
+ * host thread or several, if they use different workspaces and outputs; they
+ * give bitwise the results of the same calls run one after another.  A call
+ * uses the calling thread's current device; if no context is current on the
+ * thread it makes the device's primary context current (a context the caller
+ * made current is left in place).  The profiler (kd_profile_*) and the
+ * no-alloc entry point's shared buffer are the exceptions (see there).
  */
 #ifndef KD_TOPK_KL_H
 #define KD_TOPK_KL_H
