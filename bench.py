@@ -56,13 +56,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 
 # ------------------------------------------------------------------ helpers
 def load_peaks() -> tuple:
+    """The measured peaks of this machine's B300, else the fallback figures;
+    a measured file without a figure takes the fallback for it (and says so)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return p, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+    missing = [k for k in FALLBACK_PEAKS if not isinstance(p.get(k), (int, float))]
+    for k in missing:
+        p[k] = FALLBACK_PEAKS[k]
+    return p, "measured" if not missing else "measured, fallback for " + ", ".join(missing)
 
 
 GEMM_SOURCES = ("kd_args.h", "kd_gemm.cuh", "kd_ptx.cuh")
