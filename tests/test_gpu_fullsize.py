@@ -19,6 +19,10 @@ oracle:
 * at llama3b, all of grad_hidden and grad_W against the dense oracle run
   here on the host cores.
 
+At gptoss32k the token mask is checked too: the masked loss against the
+oracle's per-token terms over the valid tokens, grad_hidden of sampled
+valid tokens against the oracle, masked rows zero.
+
 Also: every gathered id on every row equals the cached id (bit-exact), the
 loss is the mean of the per-token terms, and grad_W satisfies two
 identities that hold at any size (its vocabulary rows sum to zero;
@@ -218,3 +222,53 @@ def test_gptoss32k_other_plans_against_oracle(flag):
     err = rel_l2(gW[vrows].cpu().numpy(), fx["grad_W_rows"].astype(np.float64))
     assert err <= GRAD_REL_L2, err
     assert torch.isfinite(gh).all()
+
+
+def test_gptoss32k_masked_against_oracle():
+    """The token mask at the headline size.  A mask leaves every token's KL
+    term unchanged and takes the mean over the valid tokens, so the stored
+    oracle terms give the masked loss; grad_hidden of sampled valid tokens
+    against the oracle normalised by the valid count, masked rows zero, and
+    grad_W's two identities."""
+    ensure_lib()
+    cfg = workloads.CONFIGS["gptoss32k"]
+    fx = load_fixture("gptoss32k")
+    inp_cpu = workloads.make_inputs_host(cfg, seed=int(fx["seed"]))
+    assert workloads.input_digest(inp_cpu) == str(fx["digest"])
+    N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
+    g = torch.Generator().manual_seed(11)
+    mask_cpu = (torch.rand(N, generator=g) < 0.6).to(torch.uint8)
+    mask_cpu[0] = 1
+    n_valid = int(mask_cpu.sum())
+    inp = to_device(inp_cpu)
+    gh = torch.empty((N, H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, cfg.chunk, 0),
+                     dtype=torch.uint8, device="cuda")
+    loss = kd.kd_topk_kl_fwd_bwd_flags(inp["hidden"], inp["W"], inp["topk_idx"],
+                                       inp["topk_logit"], mask_cpu.cuda(), T, cfg.chunk, 0, gh,
+                                       gW, ws)
+    torch.cuda.synchronize()
+    del ws
+    valid = mask_cpu.numpy().astype(bool)
+    want_loss = float(fx["loss_rows"].astype(np.float64)[valid].sum() / n_valid)
+    assert abs(loss - want_loss) <= LOSS_RTOL * abs(want_loss), (loss, want_loss)
+
+    masked_rows = torch.from_numpy(np.flatnonzero(~valid)).cuda()
+    assert int(torch.count_nonzero(gh[masked_rows])) == 0
+    rows = _sample_rows(cfg, inp_cpu["topk_logit"])
+    rows = rows[valid[rows]]
+    want = oracle.rows_forward(inp_cpu["hidden"][rows], inp_cpu["W"], inp_cpu["topk_idx"][rows],
+                               inp_cpu["topk_logit"][rows], T, N_total=n_valid)
+    rt = torch.from_numpy(rows).cuda()
+    assert rel_l2(gh[rt].cpu().numpy(), want["grad_hidden"]) <= GRAD_REL_L2
+
+    h = inp["hidden"]
+    assert torch.isfinite(gW).all()
+    col = gW.double().sum(dim=0)
+    scale = h.double().abs().sum(dim=0) * (2.0 / (T * n_valid))
+    assert float((col.abs() / scale).max()) <= 1e-3
+    a = float((gW.double() * inp["W"].double()).sum())
+    b = float((gh.double() * h.double()).sum())
+    mag = float((gh.double() * h.double()).abs().sum())
+    assert abs(a - b) <= 1e-3 * mag, (a, b, mag)
