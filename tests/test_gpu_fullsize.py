@@ -19,9 +19,11 @@ oracle:
 * at llama3b, all of grad_hidden and grad_W against the dense oracle run
   here on the host cores.
 
-At gptoss32k the token mask is checked too: the masked loss against the
-oracle's per-token terms over the valid tokens, grad_hidden of sampled
-valid tokens against the oracle, masked rows zero.
+At gptoss32k the token mask and the sharded entry point are checked too:
+the masked loss against the oracle's per-token terms over the valid
+tokens, grad_hidden of sampled valid tokens against the oracle, masked rows
+zero; two token shards normalised by the batch add up to the oracle's loss
+and grad_W rows.
 
 Also: every gathered id on every row equals the cached id (bit-exact), the
 loss is the mean of the per-token terms, and grad_W satisfies two
@@ -272,3 +274,39 @@ def test_gptoss32k_masked_against_oracle():
     b = float((gh.double() * h.double()).sum())
     mag = float((gh.double() * h.double()).abs().sum())
     assert abs(a - b) <= 1e-3 * mag, (a, b, mag)
+
+
+def test_gptoss32k_two_shards_against_oracle():
+    """The batch as two token shards, each normalised by the whole batch's
+    N and adding into one grad_W: the shards' losses add up to the oracle's
+    loss and the accumulated grad_W matches the oracle's stored rows."""
+    ensure_lib()
+    cfg = workloads.CONFIGS["gptoss32k"]
+    fx = load_fixture("gptoss32k")
+    inp_cpu = workloads.make_inputs_host(cfg, seed=int(fx["seed"]))
+    assert workloads.input_digest(inp_cpu) == str(fx["digest"])
+    N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
+    inp = to_device(inp_cpu)
+    gh = torch.empty((N, H), dtype=torch.float32, device="cuda")
+    gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+    cut = 3 * cfg.chunk + 517                      # unequal shards; a ragged last chunk in each
+    total = 0.0
+    for k, (r0, r1) in enumerate(((0, cut), (cut, N))):
+        n = r1 - r0
+        ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(n, H, V, K, cfg.chunk, 0),
+                         dtype=torch.uint8, device="cuda")
+        flags = kd.KD_FLAG_ACCUMULATE if k else 0
+        total += kd.kd_topk_kl_fwd_bwd_sharded(inp["hidden"][r0:r1], inp["W"],
+                                               inp["topk_idx"][r0:r1], inp["topk_logit"][r0:r1],
+                                               None, T, cfg.chunk, flags, N, gh[r0:r1], gW, ws)
+        del ws
+    torch.cuda.synchronize()
+    want_loss = float(fx["loss"])
+    assert abs(total - want_loss) <= LOSS_RTOL * abs(want_loss), (total, want_loss)
+    vrows = torch.from_numpy(fx["vrows"]).cuda()
+    assert rel_l2(gW[vrows].cpu().numpy(), fx["grad_W_rows"].astype(np.float64)) <= GRAD_REL_L2
+    rows = _sample_rows(cfg, inp_cpu["topk_logit"])
+    want = oracle.rows_forward(inp_cpu["hidden"][rows], inp_cpu["W"], inp_cpu["topk_idx"][rows],
+                               inp_cpu["topk_logit"][rows], T, N_total=N)
+    rt = torch.from_numpy(rows).cuda()
+    assert rel_l2(gh[rt].cpu().numpy(), want["grad_hidden"]) <= GRAD_REL_L2
