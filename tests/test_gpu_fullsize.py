@@ -287,7 +287,9 @@ def test_gptoss32k_two_shards_against_oracle():
     assert workloads.input_digest(inp_cpu) == str(fx["digest"])
     N, H, V, K, T = cfg.N, cfg.H, cfg.V, cfg.K, cfg.T
     inp = to_device(inp_cpu)
-    gh = torch.empty((N, H), dtype=torch.float32, device="cuda")
+    # KD_FLAG_ACCUMULATE adds into grad_hidden as well as grad_W: the second
+    # shard's rows must start from zero
+    gh = torch.zeros((N, H), dtype=torch.float32, device="cuda")
     gW = torch.empty((V, H), dtype=torch.float32, device="cuda")
     cut = 3 * cfg.chunk + 517                      # unequal shards; a ragged last chunk in each
     total = 0.0
