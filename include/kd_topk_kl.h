@@ -27,8 +27,8 @@
  * Arithmetic.  hidden and W are bf16; the GEMMs run on tcgen05 tensor cores
  * with fp32 accumulation; each token's logsumexp and dot product with the
  * teacher are fp32, its loss term is combined and the terms summed in
- * double; dZ is held as bf16 scratch for two consecutive
- * chunks (2 x chunk x V; one chunk with KD_FLAG_MIN_SCRATCH); grad_W is
+ * double; dZ is held as bf16 scratch for two consecutive chunks
+ * (2 x chunk x V; one chunk with KD_FLAG_MIN_SCRATCH); grad_W is
  * accumulated over those chunk pairs in fp32 in device memory.
  *
  * Pointers.  Unless stated otherwise every array argument is a DEVICE
@@ -208,7 +208,9 @@ kd_status kd_topk_kl_fwd_bwd_flags(const void* hidden, const void* W, const int3
  *   grad_W       this shard's share, scaled by 1/(T n_norm); the batch's
  *                grad_W is the sum of the shards' (add them with
  *                KD_FLAG_ACCUMULATE on one device, or an all-reduce across
- *                devices)
+ *                devices).  KD_FLAG_ACCUMULATE adds into grad_hidden too: a
+ *                shard that accumulates grad_W needs its grad_hidden rows
+ *                to hold zeros (or what they should be added to) on entry
  *   n_norm       >= 1: the number of tokens the batch's mean runs over (with
  *                masks, the batch's valid tokens); KD_ERR_INVALID_ARG otherwise
  *
