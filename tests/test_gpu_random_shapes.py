@@ -3,7 +3,8 @@
 Each case draws N, H, V, K, chunk and T at random (small enough for the
 oracle to finish in well under a second), and one of the call's modes: the
 default plan, the per-chunk grad_W plan, the stored-logits backward, a token
-mask, accumulation into non-zero gradients.  The shapes land on every kind of
+mask, accumulation into non-zero gradients, two token shards normalised by
+the whole batch (the second adding into the first's grad_W).  The shapes land on every kind of
 boundary the kernels have: chunks that are not multiples of the 256-row tile
 (so a chunk's recompute and the next chunk's forward share tiles' row ranges
 differently), odd chunk counts (a lone last chunk in its grad_W pair),
@@ -20,7 +21,7 @@ from tests.gpu_util import GRAD_REL_L2, LOSS_RTOL, ensure_lib, rel_l2, to_device
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["default", "min_scratch", "store_logits", "masked", "accumulate"]
+MODES = ["default", "min_scratch", "store_logits", "masked", "accumulate", "sharded"]
 
 
 def _case(i):
@@ -37,7 +38,7 @@ def _case(i):
     return cfg, mode
 
 
-@pytest.mark.parametrize("i", range(30))
+@pytest.mark.parametrize("i", range(36))
 def test_random_shape_against_oracle(i):
     ensure_lib()
     cfg, mode = _case(i)
@@ -57,12 +58,27 @@ def test_random_shape_against_oracle(i):
     gW0 = torch.randn((V, H), generator=g0, device="cuda") * 1e-4 if mode == "accumulate" \
         else torch.zeros((V, H), device="cuda")
     gh, gW = gh0.clone(), gW0.clone()
-    ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, cfg.chunk, flags),
-                     dtype=torch.uint8, device="cuda")
-    loss = kd.kd_topk_kl_fwd_bwd_flags(inp["hidden"], inp["W"], inp["topk_idx"],
-                                       inp["topk_logit"],
-                                       None if mask_cpu is None else mask_cpu.cuda(), cfg.T,
-                                       cfg.chunk, flags, gh, gW, ws)
+    if mode == "sharded":
+        # a random cut; the shards' rows of grad_hidden start at zero (the
+        # accumulate flag of the second shard adds into them too)
+        cut = int(np.random.default_rng(i).integers(1, N)) if N > 1 else 1
+        loss = 0.0
+        for k, (r0, r1) in enumerate(((0, cut), (cut, N))):
+            if r1 <= r0:
+                continue
+            f = kd.KD_FLAG_ACCUMULATE if r0 > 0 else 0
+            ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(r1 - r0, H, V, K, cfg.chunk, f),
+                             dtype=torch.uint8, device="cuda")
+            loss += kd.kd_topk_kl_fwd_bwd_sharded(
+                inp["hidden"][r0:r1], inp["W"], inp["topk_idx"][r0:r1],
+                inp["topk_logit"][r0:r1], None, cfg.T, cfg.chunk, f, N, gh[r0:r1], gW, ws)
+    else:
+        ws = torch.empty(kd.kd_topk_kl_workspace_size_flags(N, H, V, K, cfg.chunk, flags),
+                         dtype=torch.uint8, device="cuda")
+        loss = kd.kd_topk_kl_fwd_bwd_flags(inp["hidden"], inp["W"], inp["topk_idx"],
+                                           inp["topk_logit"],
+                                           None if mask_cpu is None else mask_cpu.cuda(), cfg.T,
+                                           cfg.chunk, flags, gh, gW, ws)
     torch.cuda.synchronize()
     want = oracle.fused_topk_kl(inp_cpu["hidden"], inp_cpu["W"], inp_cpu["topk_idx"],
                                 inp_cpu["topk_logit"], cfg.T, mask=mask_cpu)
